@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--ctx", type=int, default=0, help="override every context length (profiling)")
     ap.add_argument("--bs", type=int, default=0, help="override the block size (profiling)")
     ap.add_argument("--splits", type=int, default=0, help="override the planner's split count (0: plan it)")
+    ap.add_argument("--no-other-configs", action="store_true", help="time only the headline workload")
+    ap.add_argument("--other-steps", type=int, default=50, help="timed replays of each other workload")
     return ap.parse_args()
 
 
@@ -89,33 +91,34 @@ def job_tbps(nbytes_per_rank: int, world: int, ms: float) -> float:
     return nbytes_per_rank * world / (ms * 1e-3) / 1e12
 
 
-# DRAM traffic of the dominant kernel, from the committed ncu summary of the same kernel and
-# workload: valid only while the kernel's sources hash to the value recorded with the capture.
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "partial_tc_fp8_mtp4_fp8_ctx200k.md")
-TRAFFIC_SOURCES = ["partial_tc_fp8.cu", "tc_ptx.cuh", "common.cuh"]
-TRAFFIC_WORKLOAD = "mtp4_fp8_b200_ctx200000_bs16"
+# DRAM traffic of the dominant kernel, from the record written next to its ncu capture: valid
+# only while the kernel's sources hash to the value recorded with the capture.
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "traffic_record.json")
+
+
+def source_hash(sources):
+    import hashlib
+    h = hashlib.sha256()
+    for f in sources:
+        with open(os.path.join(ROOT, "split_kv_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def recorded_traffic(kernel, workload_name, nbytes):
     """Bytes read + written by one partial launch (ncu's dram__bytes_read.sum +
     dram__bytes_write.sum), scaled from the recorded traffic / algorithmic ratio; None when the
     kernel, the workload or the kernel sources differ from the capture."""
-    import hashlib
     from split_kv_paged_gb300 import binding as B
-    if kernel != B.TLLM_KERNEL_TC_FP8 or workload_name != TRAFFIC_WORKLOAD or not os.path.exists(TRAFFIC_PROFILE):
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    rec = {}
-    for line in open(TRAFFIC_PROFILE):
-        line = line.strip()
-        if line.startswith("traffic-record:"):
-            rec = dict(kv.split("=", 1) for kv in line.split()[1:])
-    if not rec:
+    names = {"partial_tc_fp8": B.TLLM_KERNEL_TC_FP8}
+    if names.get(rec.get("kernel")) != kernel or rec.get("workload") != workload_name:
         return None
-    h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "split_kv_paged_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest() != rec.get("source_sha256"):
+    if source_hash(rec["sources"]) != rec.get("source_sha256"):
         return None
     return float(rec["traffic_over_algorithmic"]) * nbytes
 
@@ -280,6 +283,117 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+class Measured:
+    """One workload on the device: its inputs, plan, workspace and output, and CUDA-graph
+    timings of the whole call, the partial kernel alone and the combine kernel alone.
+
+    Each timed unit is one call captured as a CUDA graph and replayed ("[FlyDSL]
+    perf(pa_decode)", Performance: CUDA events around a graph of one call), so the host's
+    launch work never sits between the events. Inputs smaller than twice the L2 would be
+    served from L2 on the next step: then every timed replay is preceded (outside its events)
+    by a write of a buffer twice the L2 size."""
+
+    def __init__(self, wl, seed, dev, stream, kernel, splits=0):
+        from split_kv_paged_gb300 import binding as B
+        self.B = B
+        self.wl, self.dev, self.stream = wl, dev, stream
+        self.inp = W.make_inputs(wl, seed, device=dev)
+        desc = B.desc_for(wl, kernel, num_pages=self.inp.num_pages)
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        plan_args = (desc, wl.B, wl.Lq, wl.window)
+        plan_kw = dict(host_ctx_lens=wl.ctx, num_sms=n_sm, splits_override=splits)
+        self.plan = B.tllm_decode_attn_plan(*plan_args, **plan_kw)
+        # host time of the planner (the call a serving loop makes when the shape changes)
+        reps = 200
+        t = time.perf_counter()
+        for _ in range(reps):
+            B.tllm_decode_attn_plan(*plan_args, **plan_kw)
+        self.plan_us = (time.perf_counter() - t) / reps * 1e6
+        self.ws = B.Workspace(self.plan, device=dev)
+        self.out = torch.empty((wl.B, wl.Lq, wl.Hq, wl.D), dtype=W.DTYPES[wl.out_dtype], device=dev)
+        self.S = self.plan.num_splits
+        self.nbytes = W.effective_bytes(wl)
+        l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
+        self.flush_buf = None
+        if self.nbytes < 2 * l2_bytes:
+            self.flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
+            self.l2_note = (f"inputs ({self.nbytes / 1e9:.3f} GB) smaller than 2x L2: L2 flushed by a "
+                            f"{2 * l2_bytes >> 20} MiB write before every timed step")
+        else:
+            self.l2_note = f"inputs ({self.nbytes / 1e9:.2f} GB) larger than L2; no flush"
+        inp = self.inp
+        self.call = (inp.q, inp.k_cache, inp.v_cache, inp.block_table, inp.context_lens, wl.Lq, inp.kv_scales,
+                     inp.sinks, wl.window, self.S, self.ws, self.out)
+
+    def capture(self, warmup):
+        B, stream = self.B, self.stream
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                B.tllm_decode_attn_splitkv(*self.call, stream=stream)
+            torch.cuda.synchronize(self.dev)
+
+            def graph(fn):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                return g
+            self.g_call = graph(lambda: B.tllm_decode_attn_splitkv(*self.call, stream=stream))
+            self.g_part = graph(lambda: B.tllm_decode_attn_partial(*self.call, stream=stream))
+            self.g_comb = graph(lambda: B.tllm_decode_attn_combine(*self.call, stream=stream)) if self.S > 1 else None
+            for g in (self.g_call, self.g_part, self.g_comb):
+                if g is not None:
+                    for _ in range(max(1, warmup)):
+                        g.replay()
+            torch.cuda.synchronize(self.dev)
+
+    def timed(self, g, K):
+        """K replays of g. Returns (mean ms per replay over the K, median over three
+        consecutive runs of K/3 replays of each run's mean ms)."""
+        stream = self.stream
+        with torch.cuda.stream(stream):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(K):
+                if self.flush_buf is not None:
+                    self.flush_buf.fill_(k)
+                ev[k][0].record(stream)
+                g.replay()
+                ev[k][1].record(stream)
+            e1.record(stream)
+            torch.cuda.synchronize(self.dev)
+        per = [x.elapsed_time(y) for x, y in ev]
+        mean = e0.elapsed_time(e1) / K if self.flush_buf is None else sum(per) / K
+        runs = [per[i * K // 3:(i + 1) * K // 3] for i in range(3)] if K >= 3 else [per]
+        med3 = statistics.median(sum(r) / len(r) for r in runs if r)
+        return mean, med3
+
+    def release(self):
+        for name in ("inp", "ws", "out", "flush_buf", "g_call", "g_part", "g_comb", "call"):
+            if hasattr(self, name):
+                delattr(self, name)
+        torch.cuda.empty_cache()
+
+
+def other_config(name, wl, seed, dev, stream, peak, steps, warmup, splits=0):
+    """µs per call, TB/s and fraction of the HBM peak of one more workload (graph replays,
+    L2 flushed before each step when its inputs are small)."""
+    from split_kv_paged_gb300 import binding as B
+    m = Measured(wl, seed, dev, stream, B.TLLM_KERNEL_AUTO, splits)
+    m.capture(warmup)
+    call_ms, call_med = m.timed(m.g_call, steps)
+    part_ms, _ = m.timed(m.g_part, steps)
+    comb_ms = m.timed(m.g_comb, steps)[0] if m.g_comb is not None else 0.0
+    tbps = m.nbytes / (call_ms * 1e-3) / 1e12
+    rec = {"workload": wl.name, "num_splits": m.S, "kernel": int(m.plan.kernel), "logical_bytes": m.nbytes,
+           "us_per_call": call_ms * 1e3, "us_per_call_median_of_3_runs": call_med * 1e3, "TBps": tbps,
+           "frac": tbps * 1e3 / peak, "partial_us": part_ms * 1e3, "combine_alone_us": comb_ms * 1e3,
+           "partial_frac": m.nbytes / (part_ms * 1e-3) / 1e9 / peak, "plan_host_us": m.plan_us,
+           "steps": steps, "l2": m.l2_note}
+    m.release()
+    return name, rec
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -295,81 +409,23 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wl = workload(args)
-    inp = W.make_inputs(wl, rank_seed(rank), device=dev)
-    desc = B.desc_for(wl, kernel_code(args.kernel), num_pages=inp.num_pages)
-    plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx,
-                                   num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
-                                   splits_override=args.splits)
-    ws = B.Workspace(plan, device=dev)
-    out = torch.empty((wl.B, wl.Lq, wl.Hq, wl.D), dtype=W.DTYPES[wl.out_dtype], device=dev)
-    S = plan.num_splits
-    nbytes = W.effective_bytes(wl)
     stream = torch.cuda.Stream(device=dev)
-    # Inputs smaller than twice the L2 would be served from L2 on the next step: then every timed
-    # step is preceded (outside its events) by a write of a buffer twice the L2 size.
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
-    flush_buf = None
-    if nbytes < 2 * l2_bytes:
-        flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
-        l2_note = f"inputs ({nbytes / 1e9:.3f} GB) smaller than 2x L2: L2 flushed by a {2 * l2_bytes >> 20} MiB write before every timed step"
-    else:
-        l2_note = f"inputs ({nbytes / 1e9:.2f} GB) larger than L2; no flush"
-    call = (inp.q, inp.k_cache, inp.v_cache, inp.block_table, inp.context_lens, wl.Lq, inp.kv_scales, inp.sinks,
-            wl.window, S, ws, out)
+    m = Measured(wl, rank_seed(rank), dev, stream, kernel_code(args.kernel), args.splits)
+    plan, inp, out, S, nbytes = m.plan, m.inp, m.out, m.S, m.nbytes
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            B.tllm_decode_attn_splitkv(*call, stream=stream)
-        torch.cuda.synchronize(dev)
-        # Each timed unit is one call captured as a CUDA graph and replayed ("[FlyDSL]
-        # perf(pa_decode)", Performance: CUDA events around a graph of one call), so the host's
-        # launch work never sits between the events: the whole call (partial + combine, as
-        # tllm_decode_attn_splitkv launches them), the partial kernel alone (its roofline line)
-        # and the combine kernel alone.
-        def capture(fn):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-            return g
-        g_call = capture(lambda: B.tllm_decode_attn_splitkv(*call, stream=stream))
-        g_part = capture(lambda: B.tllm_decode_attn_partial(*call, stream=stream))
-        g_comb = capture(lambda: B.tllm_decode_attn_combine(*call, stream=stream)) if S > 1 else None
-        for g in (g_call, g_part, g_comb):
-            if g is not None:
-                for _ in range(max(1, args.warmup)):
-                    g.replay()
-        torch.cuda.synchronize(dev)
-        K = args.steps
-
-        def timed(g):
-            """K replays of g; per replay, an L2 flush (outside the events) when the inputs are
-            small. Returns the mean milliseconds per replay."""
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for k in range(K):
-                if flush_buf is not None:
-                    flush_buf.fill_(k)
-                ev[k][0].record(stream)
-                g.replay()
-                ev[k][1].record(stream)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            if flush_buf is None:
-                return e0.elapsed_time(e1) / K
-            return sum(x.elapsed_time(y) for x, y in ev) / K
-
-        barrier()
-        torch.cuda.synchronize(dev)
-        with ClockSampler(local_rank) as clocks:
-            ms_step = timed(g_call)
-        barrier()
-        partial_ms = timed(g_part)
-        combine_ms = timed(g_comb) if g_comb is not None else 0.0
+    m.capture(args.warmup)
+    K = args.steps
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        ms_step, ms_med3 = m.timed(m.g_call, K)
+    barrier()
+    partial_ms, _ = m.timed(m.g_part, K)
+    combine_ms = m.timed(m.g_comb, K)[0] if m.g_comb is not None else 0.0
     ms_step = max_over_ranks(ms_step, world, dev)
     value = job_tbps(nbytes, world, ms_step)
 
@@ -389,7 +445,7 @@ def main():
         def e2e_step():
             for k, h in host.items():
                 dev_tensors[k].copy_(h, non_blocking=True)
-            B.tllm_decode_attn_splitkv(*call, stream=stream)
+            B.tllm_decode_attn_splitkv(*m.call, stream=stream)
             out_host.copy_(out, non_blocking=True)
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -403,6 +459,7 @@ def main():
         barrier()
     e2e_ms = a.elapsed_time(b) / E
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    del host, out_host
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -411,17 +468,33 @@ def main():
                "seconds": secs}
 
     peak, peak_src = peak_hbm()
+    # the other measured workloads, each timed the same way (graph replays of one call), on
+    # rank 0 of a single-rank run by default
+    others = {}
+    if rank == 0 and world == 1 and not args.no_other_configs and args.workload == "mtp4_fp8_long" \
+            and args.batch == 0 and args.ctx == 0 and args.bs == 0:
+        k_o, w_o = args.other_steps, max(3, min(args.warmup, 5))
+        specs = [("single_decode_S1", W.single_decode(), 1001, 1), ("single_decode_S4", W.single_decode(), 1001, 4),
+                 ("verify16_int8", W.verify16_int8(), 1002, 0),
+                 ("ragged_fp8_bs128", W.ragged_fp8(bs=128), 1004, 0),
+                 ("ragged_fp8_bs16", W.ragged_fp8(bs=16), 1004, 0),
+                 ("window_sink_bf16", W.window_sink_bf16(), 1005, 0)]
+        for name, wlo, seed, splits in specs:
+            k, rec = other_config(name, wlo, seed, dev, stream, peak, k_o, w_o, splits)
+            others[k] = rec
+
     achieved = nbytes / (partial_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_call": ms_step * 1e3,
+        "us_per_call_median_of_3_runs": ms_med3 * 1e3,
         "pct_of_peak": 100.0 * value * 1e3 / world / peak, "peak_source": peak_src,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.kv_dtype,
         "data": "synthetic",
         "config": {"workload": wl.name, "batch": wl.B, "ctx": max(wl.ctx), "query_rows": wl.Lq, "Hq": wl.Hq,
                    "Hkv": wl.Hkv, "head_dim": wl.D, "block_size": wl.bs, "num_splits": S,
-                   "kernel": int(plan.kernel), "logical_bytes": nbytes,
-                   "l2": l2_note,
+                   "kernel": int(plan.kernel), "logical_bytes": nbytes, "plan_host_us": m.plan_us,
+                   "l2": m.l2_note, "aggregation": "mean of the K timed graph replays",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(int(plan.kernel), wl.name, nbytes), "kernel": "partial",
@@ -431,6 +504,8 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (2 if S > 1 else 1),
     }
+    if others:
+        line["other_configs"] = others
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:

@@ -242,8 +242,10 @@ const char* tllm_status_string(tllm_status status);
  *     workspace.
  *   - A plan whose workspace_bytes exceeds the array returns TLLM_ERR_WORKSPACE_TOO_SMALL,
  *     and nothing is launched.
+ *   - Every argument is checked first; on any error nothing is queued on `stream`.
  *   - The call allocates and frees nothing. It zeroes the array's status word on `stream`,
- *     then runs the partial and combine kernels.
+ *     then runs the partial and combine kernels. tllm_decode_attn_noalloc_read_status reads
+ *     that word afterwards.
  *   - All calls on a device share the one array, and it keeps the last call's contents.
  *     Calls that overlap on the GPU (unordered streams) race on it.
  *   - The first call on each device looks up the array's device address. Make that call
@@ -255,6 +257,18 @@ tllm_status tllm_decode_attn_splitkv_noalloc(const void* q, const void* k_cache,
                                              int32_t window, int32_t num_splits,
                                              const tllm_decode_attn_plan_t* plan, void* out,
                                              tllm_stream_t stream);
+
+/*
+ * The status word of the library-owned record area (TLLM_FLAG_*), the counterpart of
+ * tllm_decode_attn_read_status for tllm_decode_attn_splitkv_noalloc: a TLLM_FLAG_TIMEOUT
+ * here means the last no-alloc call's output is not valid. The next no-alloc call zeroes the
+ * word again, so read it after the call whose result you check. `reset` non-zero clears it.
+ * Synchronises `stream`; do not call during graph capture. No allocation.
+ */
+tllm_status tllm_decode_attn_noalloc_read_status(uint32_t* flags, int32_t reset, tllm_stream_t stream);
+
+/* TLLM_NOALLOC_SCRATCH_BYTES as built into the library (for bindings that cannot read the macro). */
+size_t tllm_decode_attn_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

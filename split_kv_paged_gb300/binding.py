@@ -92,6 +92,11 @@ def lib() -> ctypes.CDLL:
             L.tllm_decode_attn_splitkv_noalloc.restype = ctypes.c_int
             L.tllm_decode_attn_splitkv_noalloc.argtypes = _CALL_ARGS[:10] + [
                 ctypes.POINTER(tllm_decode_attn_plan_t), ctypes.c_void_p, ctypes.c_void_p]
+            L.tllm_decode_attn_noalloc_read_status.restype = ctypes.c_int
+            L.tllm_decode_attn_noalloc_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32,
+                                                               ctypes.c_void_p]
+            L.tllm_decode_attn_noalloc_scratch_bytes.restype = ctypes.c_size_t
+            L.tllm_decode_attn_noalloc_scratch_bytes.argtypes = []
             L.tllm_decode_attn_read_status.restype = ctypes.c_int
             L.tllm_decode_attn_read_status.argtypes = [ctypes.POINTER(tllm_workspace), ctypes.POINTER(ctypes.c_uint32),
                                                        ctypes.c_int32, ctypes.c_void_p]
@@ -188,7 +193,17 @@ def tllm_decode_attn_combine(q, k_cache, v_cache, block_table, context_lens, que
           window, num_splits, workspace, out, stream)
 
 
-TLLM_NOALLOC_SCRATCH_BYTES = 32 << 20
+def tllm_decode_attn_noalloc_scratch_bytes() -> int:
+    """Size of the library-owned record area of the no-alloc entry point (read from the library)."""
+    return int(lib().tllm_decode_attn_noalloc_scratch_bytes())
+
+
+def tllm_decode_attn_noalloc_read_status(reset: bool = False, stream=None) -> int:
+    """Status word (TLLM_FLAG_*) of the no-alloc entry point's record area."""
+    flags = ctypes.c_uint32()
+    _check(lib().tllm_decode_attn_noalloc_read_status(ctypes.byref(flags), int(bool(reset)), _stream_handle(stream)),
+           "tllm_decode_attn_noalloc_read_status")
+    return flags.value
 
 
 def tllm_decode_attn_splitkv_noalloc(q, k_cache, v_cache, block_table, context_lens, query_len, kv_scales, sinks,

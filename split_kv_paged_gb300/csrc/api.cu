@@ -247,8 +247,10 @@ tllm_status tllm_decode_attn_split_range(const tllm_decode_attn_plan_t* plan, in
 
 }  // extern "C"
 
-namespace {
+namespace tllm {
 
+// Checks the call arguments against the plan and, when they pass, fills the launch
+// parameters. Queues nothing and makes no CUDA call.
 tllm_status make_params(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                         const int32_t* context_lens, int32_t query_len, const float* kv_scales,
                         const float* sinks, int32_t window, int32_t num_splits, const tllm_workspace* ws,
@@ -305,29 +307,31 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->q_dtype = d.q_dtype;
   p->kv_dtype = d.kv_dtype;
   p->out_dtype = d.out_dtype;
-  return TLLM_OK;
+  // alignment the chosen kernel's copies need (TMA boxes, 16-byte loads and stores)
+  bool aligned = true;
+  switch (pl.kernel) {
+    case TLLM_KERNEL_TC_FP8: aligned = tc_fp8_pointers_ok(*p); break;
+    case TLLM_KERNEL_TC_I8: aligned = tc_i8_pointers_ok(*p); break;
+    case TLLM_KERNEL_SIMT: aligned = simt_pointers_ok(*p); break;
+    case TLLM_KERNEL_TC_B16: aligned = tc_b16_pointers_ok(*p); break;
+    default: break;
+  }
+  return aligned ? TLLM_OK : TLLM_ERR_INVALID_ARG;
 }
+
+}  // namespace tllm
+
+namespace {
 
 tllm_status run_partial(const Params& p, int kernel, cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidValue;
+  // (make_params has checked the pointers' alignment for the kernel)
   switch (kernel) {
     case TLLM_KERNEL_GENERIC: e = launch_partial_generic(p, s); break;
-    case TLLM_KERNEL_TC_FP8:
-      if (!tc_fp8_pointers_ok(p)) return TLLM_ERR_INVALID_ARG;   // TMA needs 16-byte aligned bases
-      e = launch_partial_tc_fp8(p, s);
-      break;
-    case TLLM_KERNEL_TC_I8:
-      if (!tc_i8_pointers_ok(p)) return TLLM_ERR_INVALID_ARG;    // TMA and 16-byte copies
-      e = launch_partial_tc_i8(p, s);
-      break;
-    case TLLM_KERNEL_SIMT:
-      if (!simt_pointers_ok(p)) return TLLM_ERR_INVALID_ARG;     // 16-byte asynchronous copies
-      e = launch_partial_simt(p, s);
-      break;
-    case TLLM_KERNEL_TC_B16:
-      if (!tc_b16_pointers_ok(p)) return TLLM_ERR_INVALID_ARG;   // TMA and 16-byte query loads
-      e = launch_partial_tc_b16(p, s);
-      break;
+    case TLLM_KERNEL_TC_FP8: e = launch_partial_tc_fp8(p, s); break;
+    case TLLM_KERNEL_TC_I8: e = launch_partial_tc_i8(p, s); break;
+    case TLLM_KERNEL_SIMT: e = launch_partial_simt(p, s); break;
+    case TLLM_KERNEL_TC_B16: e = launch_partial_tc_b16(p, s); break;
     default: return TLLM_ERR_UNSUPPORTED;
   }
   return e == cudaSuccess ? TLLM_OK : TLLM_ERR_CUDA;

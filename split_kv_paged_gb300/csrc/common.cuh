@@ -176,6 +176,13 @@ cudaError_t set_smem_attr(const void* func, int bytes);
 // Streaming multiprocessors of the current device (cached per device); 0 on error.
 int sm_count();
 
+// Checks the arguments of a call (tllm_decode_attn_splitkv and its stages) against the plan in
+// `ws` and fills the launch parameters; queues nothing and makes no CUDA call.
+tllm_status make_params(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                        const int32_t* context_lens, int32_t query_len, const float* kv_scales,
+                        const float* sinks, int32_t window, int32_t num_splits, const tllm_workspace* ws,
+                        void* out, Params* p);
+
 // ---- launchers (one per kernel family) ---------------------------------------------
 cudaError_t launch_partial_generic(const Params& p, cudaStream_t stream);
 cudaError_t launch_combine(const Params& p, cudaStream_t stream);

@@ -57,15 +57,36 @@ extern "C" tllm_status tllm_decode_attn_splitkv_noalloc(const void* q, const voi
                                                         tllm_stream_t stream) {
   if (!plan) return TLLM_ERR_INVALID_ARG;
   if (plan->workspace_bytes > (size_t)TLLM_NOALLOC_SCRATCH_BYTES) return TLLM_ERR_WORKSPACE_TOO_SMALL;
-  void* scratch = nullptr;
-  tllm_status st = scratch_address(&scratch);
-  if (st != TLLM_OK) return st;
-  // The status word at the head of the records starts each call at zero.
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess) return TLLM_ERR_CUDA;
+  // Every argument is checked before any CUDA call. make_params only does arithmetic on the
+  // workspace address, so an aligned stand-in serves for the check.
   tllm_workspace ws;
   ws.plan = plan;
-  ws.ptr = scratch;
+  ws.ptr = reinterpret_cast<void*>((uintptr_t)256);
   ws.bytes = TLLM_NOALLOC_SCRATCH_BYTES;
+  tllm::Params params;
+  tllm_status st = tllm::make_params(q, k_cache, v_cache, block_table, context_lens, query_len, kv_scales, sinks, window,
+                               num_splits, &ws, out, &params);
+  if (st != TLLM_OK) return st;
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != TLLM_OK) return st;
+  ws.ptr = scratch;
+  // The status word at the head of the records starts each call at zero.
+  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess) return TLLM_ERR_CUDA;
   return tllm_decode_attn_splitkv(q, k_cache, v_cache, block_table, context_lens, query_len, kv_scales, sinks,
                                   window, num_splits, &ws, out, stream);
 }
+
+extern "C" tllm_status tllm_decode_attn_noalloc_read_status(uint32_t* flags, int32_t reset, tllm_stream_t stream) {
+  if (!flags) return TLLM_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  tllm_status st = scratch_address(&scratch);
+  if (st != TLLM_OK) return st;
+  tllm_workspace ws;
+  ws.plan = nullptr;
+  ws.ptr = scratch;
+  ws.bytes = TLLM_NOALLOC_SCRATCH_BYTES;
+  return tllm_decode_attn_read_status(&ws, flags, reset, stream);
+}
+
+extern "C" size_t tllm_decode_attn_noalloc_scratch_bytes(void) { return (size_t)TLLM_NOALLOC_SCRATCH_BYTES; }

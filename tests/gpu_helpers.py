@@ -156,13 +156,29 @@ def abs_value_inputs(inp):
 
 
 def assert_close_conditioned(got: torch.Tensor, ref: np.ndarray, cond: np.ndarray, kv_dtype: str, what: str = ""):
-    """|gpu - ref| <= tol * sum_t w_t |v_t| + u * |ref|: the tolerance measured against the
-    magnitude of the terms, for outputs that are small differences of large terms."""
+    """The tolerance for outputs that are small differences of large terms.
+
+    cond = sum_t w_t |v_t| (the oracle on |V|) is the magnitude of the terms whose weighted
+    sum is the output. Elements without cancellation (cond <= 4 |ref|) must meet the plain
+    bound of assert_close, |gpu - ref| <= tol + (tol + u) |ref|. Every element must meet
+    |gpu - ref| <= tol * cond + u * |ref|: the forward error bound of a weighted sum
+    computed with relative precision tol per term, plus the output's own rounding. Returns
+    the worst ratio of error to the plain bound on the cancelling elements, for the report."""
     g = got.detach().double().cpu().numpy()
     tol = tol_for(kv_dtype)
     u = OUT_ROUNDOFF[out_name(got)]
     assert np.isfinite(g).all(), f"{what}: non-finite outputs"
     err = np.abs(g - ref)
+    plain = tol + (tol + u) * np.abs(ref)
+    calm = cond <= 4.0 * np.abs(ref)
+    bad_plain = calm & (err > plain)
+    assert not bad_plain.any(), (f"{what}: {bad_plain.sum()} of {calm.sum()} non-cancelling elements outside the "
+                                 f"plain bound; worst ratio {(err / plain)[calm].max():.3f}")
     bound = tol * cond + u * np.abs(ref) + 1e-30
     bad = err > bound
     assert not bad.any(), f"{what}: {bad.sum()} elements outside the conditioned bound; worst ratio {(err / bound).max():.3f}"
+    worst = float((err / plain)[~calm].max()) if (~calm).any() else 0.0
+    print(f"{what}: {calm.sum()} non-cancelling elements within the plain bound (worst "
+          f"{(err / plain)[calm].max() if calm.any() else 0.0:.3f}); on the {(~calm).sum()} cancelling elements "
+          f"the worst error / plain bound is {worst:.3f}, conditioned bound worst {(err / bound).max():.3f}")
+    return worst

@@ -249,7 +249,28 @@ def test_noalloc_refuses_plans_beyond_its_array(lib):
     CUDA call."""
     wl = W.mtp4_fp8_long()
     plan = _plan(wl, host_ctx_lens=wl.ctx, splits_override=16)     # 105 MB of split records
-    assert plan.workspace_bytes > B.TLLM_NOALLOC_SCRATCH_BYTES
+    assert plan.workspace_bytes > B.tllm_decode_attn_noalloc_scratch_bytes()
     st = B.lib().tllm_decode_attn_splitkv_noalloc(256, 256, 256, 256, 256, wl.Lq, 256, None, 0, plan.num_splits,
                                                   ctypes.byref(plan), 256, None)
     assert st == B.TLLM_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_array_size_matches_the_header(lib):
+    """The size the library reports for its record area is the header's macro."""
+    text = open(os.path.join(ROOT, "include", "tllm_decode_attn.h")).read()
+    m = re.search(r"#define\s+TLLM_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "macro not found"
+    assert B.tllm_decode_attn_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_checks_arguments_before_queueing_anything(lib):
+    """A bad argument to the no-alloc entry point returns its status before any work is queued:
+    the status word of the record area (zeroed at each call start) is not touched, so the call
+    needs no GPU to fail."""
+    wl = W.mtp4_fp8_long(batch=2, ctx=3000)
+    plan = _plan(wl, host_ctx_lens=wl.ctx, splits_override=2)
+    # a null query pointer, then a misaligned one (the FP8 tensor-core kernel needs 16 bytes)
+    for q in (None, 258):
+        st = B.lib().tllm_decode_attn_splitkv_noalloc(q, 256, 256, 256, 256, wl.Lq, 256, None, 0, 2,
+                                                      ctypes.byref(plan), 256, None)
+        assert st == B.TLLM_ERR_INVALID_ARG

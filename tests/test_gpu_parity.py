@@ -109,14 +109,32 @@ def test_window_sink_graph_replay():
         assert_close(out, ref, wl.kv_dtype, f"replay {rep} ctx[:4]={ctx[:4]}")
 
 
+def persistent_pass_requests(plan, n_sm: int):
+    """Requests whose split items open and close each pass of the persistent grid: the
+    kernels give CTA c the items c, c + grid, c + 2 grid, ... of the (request x kv head,
+    split) list, so pass k covers items [k grid, (k + 1) grid)."""
+    S, Hkv = plan.num_splits, plan.desc.num_kv_heads
+    n_items = plan.batch * Hkv * S
+    grid = min(n_items, n_sm)
+    idx = set()
+    for first in range(0, n_items, grid):
+        last = min(n_items, first + grid) - 1
+        idx.add(first // S // Hkv)
+        idx.add(last // S // Hkv)
+        idx.add((first + last) // 2 // S // Hkv)
+    return sorted(idx)
+
+
 def test_mtp4_fp8_full_size_sampled():
     """The full batch-200 x 200,000 workload in the launch configuration the benchmark
-    times; the oracle checks three whole requests (first, middle, last)."""
+    times; the oracle checks whole requests from every pass of the persistent grid (the
+    first, middle and last request of each pass)."""
     wl = W.mtp4_fp8_long()
     inp = W.make_inputs(wl, 1003, device="cuda")
     out, plan, _ = run_gpu(inp)
     assert plan.num_splits > 1
-    idx = [0, 99, 199]
+    idx = persistent_pass_requests(plan, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert 8 <= len(idx) <= 16, idx
     sub = W.gather_requests(inp, idx)
     ref, _ = oracle_out(sub)
     assert_close(out[idx], ref, wl.kv_dtype, "full-size sampled")
