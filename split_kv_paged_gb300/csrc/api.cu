@@ -34,12 +34,13 @@ tllm_status check_desc(const tllm_decode_attn_desc* d) {
 }
 
 // Planning traits of a kernel variant: tokens per tile (split boundaries align to it),
-// resident CTAs per SM, CTAs per (request, kv head, split), and the fixed cost of one CTA
-// (set-up, pipeline fill, epilogue) expressed in tokens of streaming. hbm_bound: one CTA
-// alone streams faster than its share of HBM, so when some SMs run out of work the others
-// speed up; its time then follows the work per SM (but no less than the longest item), not
-// the number of waves. combine_tokens: the in-call cost of the combine launch that a plan
-// with more than one split adds.
+// resident CTAs per SM, CTAs per (request, kv head, split), and the fixed cost of one CTA or
+// item (set-up, pipeline fill, epilogue) expressed in tokens of streaming. persistent: CTAs
+// take the items of the device work list in turn (item k to CTA k mod grid), so the plan can
+// simulate each CTA's load. hbm_bound: one CTA alone streams faster than its share of HBM, so
+// when some SMs run out of work the others speed up; its time then follows the work per SM
+// (but no less than the longest item), not the number of waves. combine_tokens: the in-call
+// cost of the combine launch that a plan with more than one split adds.
 struct KernelTraits {
   int tile;
   int ctas_per_sm;
@@ -47,17 +48,39 @@ struct KernelTraits {
   int overhead_tokens;
   bool hbm_bound = false;
   int combine_tokens = 0;
+  bool persistent = false;
 };
 
 KernelTraits traits(int kernel, const tllm_decode_attn_desc& d, int rows) {
 
   switch (kernel) {
-    case TLLM_KERNEL_TC_FP8: return KernelTraits{128, 1, 1, 1024};
+    case TLLM_KERNEL_TC_FP8: return KernelTraits{128, 1, 1, 1024, false, 512, true};
     case TLLM_KERNEL_SIMT: return KernelTraits{simt_tile(d.head_dim), 2, 1, 256};
-    case TLLM_KERNEL_TC_I8: return KernelTraits{64, 1, 1, 512};
+    case TLLM_KERNEL_TC_I8: return KernelTraits{64, 1, 1, 512, false, 128, true};
     case TLLM_KERNEL_TC_B16: return KernelTraits{128, 1, 1, 256, true, 700};
     default: return KernelTraits{32, 2, (rows + 15) / 16, 64};
   }
+}
+
+// Busiest CTA of a persistent kernel, in tokens of streaming: the items of the work list
+// (unit-major, each split's tiles plus the fixed cost of an item) dealt to `grid` CTAs in turn.
+double persistent_cost(const std::vector<int>& ctx, int Lq, int window, int S, int min_chunk, int align, int Hkv,
+                       int tile, double overhead, int grid, std::vector<double>& load) {
+  load.assign(grid, 0.0);
+  int64_t k = 0;
+  for (int c : ctx) {
+    const Span sp = request_span(c, Lq, window, S, min_chunk, align);
+    for (int g = 0; g < Hkv; g++) {
+      for (int s = 0; s < sp.nsplit; s++, k++) {
+        const int t0 = sp.base + s * sp.chunk, t1 = std::min(c, t0 + sp.chunk);
+        const int tiles = t1 > t0 ? (t1 - t0 + tile - 1) / tile : 0;
+        load[k % grid] += (double)tiles * tile + overhead;
+      }
+    }
+  }
+  double mx = 0.0;
+  for (double v : load) mx = std::max(mx, v);
+  return mx;
 }
 
 bool kernel_supports(int kernel, const tllm_decode_attn_desc& d, int rows) {
@@ -173,8 +196,52 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
   }
   const int s_cap = std::max(1, std::min(kMaxSplits, (max_vis + min_chunk - 1) / min_chunk));
   int S = 1;
+  int chunk_floor = min_chunk;             // the plan's smallest split (tokens)
   if (splits_override > 0) {
     S = std::min(splits_override, kMaxSplits);
+  } else if (kt.persistent) {
+    // Work-based choice for the persistent kernels (aiter PR #5628, Changes: partitions sized
+    // from the known KV work rather than a fixed CTA budget). A candidate is a split size c:
+    // every request is cut into ceil(visible / c) splits of c tokens (S = the most any request
+    // needs), and the work list deals the items to the CTAs in turn. Its estimated time is the
+    // busiest CTA's load, plus the combine when any request splits. The candidates are the
+    // even cuts of the longest request into s = 1 .. s_cap parts and the cuts that spread all
+    // the work evenly over one to eight item waves. Ties go to fewer splits.
+    const int slots = num_sms * kt.ctas_per_sm;
+    int64_t total = 0;
+    for (int c : ctx) total += (int64_t)(c - request_span(c, query_len, window, 1, align, align).base) * d.num_kv_heads;
+    std::vector<int> cands;
+    auto roundup = [&](int64_t x) { return (int)std::min<int64_t>(max_ctx, ((x + align - 1) / align) * align); };
+    for (int s = 1; s <= s_cap; s++) cands.push_back(std::max(min_chunk, roundup((max_vis + s - 1) / s)));
+    for (int w = 1; w <= 8; w++)
+      cands.push_back(std::max(min_chunk, roundup((total + (int64_t)slots * w - 1) / ((int64_t)slots * w))));
+    std::vector<std::pair<int, int>> options;        // (S, c)
+    for (int c : cands) {
+      int sc = 1;
+      for (int x : ctx) {
+        const int vis = x - request_span(x, query_len, window, 1, align, align).base;
+        sc = std::max(sc, (vis + c - 1) / c);
+      }
+      options.emplace_back(std::min(sc, kMaxSplits), c);
+    }
+    std::sort(options.begin(), options.end());
+    options.erase(std::unique(options.begin(), options.end()), options.end());
+    std::vector<double> load;
+    double best = 1e300;
+    for (auto [sc, c] : options) {
+      int64_t items = 0;
+      for (int x : ctx) items += (int64_t)request_span(x, query_len, window, sc, c, align).nsplit * d.num_kv_heads;
+      if (items > 32 * (int64_t)slots && sc > 1) continue;         // items too small for their fixed cost
+      const int grid = (int)std::min<int64_t>((int64_t)batch * d.num_kv_heads * sc, slots);
+      const double cost = persistent_cost(ctx, query_len, window, sc, c, align, d.num_kv_heads, kt.tile,
+                                          kt.overhead_tokens, grid, load) +
+                          (sc > 1 ? kt.combine_tokens : 0);
+      if (cost < best * 0.999) {
+        best = cost;
+        S = sc;
+        chunk_floor = c;
+      }
+    }
   } else {
     // Work-based choice: estimated time = waves x (chunk + per-CTA overhead), where a
     // wave is num_sms * ctas_per_sm CTAs; for an HBM-bound kernel, the tokens per slot (at
@@ -210,7 +277,7 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
   out_plan->window = window;
   out_plan->num_splits = S;
   out_plan->max_splits = S;
-  out_plan->min_chunk = min_chunk;
+  out_plan->min_chunk = chunk_floor;
   out_plan->split_align = align;
   out_plan->kernel = kernel;
   out_plan->rows = rows;

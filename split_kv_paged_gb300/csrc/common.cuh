@@ -79,6 +79,68 @@ TLLM_HD Span request_span(int ctx, int Lq, int window, int num_splits, int min_c
   return s;
 }
 
+// ---- the work list of the persistent partial kernels ----------------------------------
+// The real items of a call are the (unit = request x kv head, split) pairs with split below
+// the number of splits the unit's request uses (from its device-side length), in unit-major
+// order; CTA c of a grid of G CTAs takes the items of rank c, c + G, c + 2 G, ... So every CTA
+// gets real work while there is any, and a request's unused split slots cost nothing (aiter
+// PR #5628, Changes: a work plan built on the GPU from the lengths, with capacity fixed for
+// graph replay).
+//
+// build_work_list writes into shared memory the items of this CTA whose rank lies in
+// [round0, round0 + kListCap) of its own sequence: entry i is (unit << 8) | split of the
+// item of rank c + G (round0 + i), and entry kListCap + i the request's context length as
+// read from context_lens (not yet clamped). It returns how many items it wrote (the same value
+// in every thread). Every thread of the CTA calls it; it ends with a CTA barrier, after which
+// the list is read-only until the next call. `list` holds kListWords ints: the two arrays and
+// one int of scan scratch per warp.
+constexpr int kListCap = 64;
+constexpr int kListWords = 2 * kListCap + 32;
+
+__device__ __forceinline__ int build_work_list(const Params& p, int* list, int round0) {
+  int* scan = list + 2 * kListCap;
+  const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int U = p.B * p.Hkv;
+  int base = 0;                                     // real items in the units before this chunk
+  for (int u0 = 0; u0 < U; u0 += nthr) {
+    const int u = u0 + tid;
+    int n = 0, raw = 0;
+    if (u < U) {
+      raw = p.context_lens[u / p.Hkv];
+      n = request_span(clamp_ctx(raw, p.max_ctx), p.Lq, p.window, p.num_splits, p.min_chunk, p.align).nsplit;
+    }
+    int incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    int wofs = 0, total = 0;
+    for (int w = 0; w < nwarps; w++) {
+      const int v = scan[w];
+      wofs += w < warp ? v : 0;
+      total += v;
+    }
+    const int first = base + wofs + incl - n;       // rank of (u, split 0)
+    int k = first + ((c - first % G) % G + G) % G;  // smallest rank >= first owned by this CTA
+    for (; k < first + n; k += G) {
+      const int i = k / G - round0;
+      if (i >= 0 && i < kListCap) {
+        list[i] = (u << 8) | (k - first);
+        list[kListCap + i] = raw;
+      }
+    }
+    base += total;
+    __syncthreads();                                // scan reused; the list complete after the last chunk
+  }
+  const int mine = base > c ? (base - c + G - 1) / G : 0;
+  const int left = mine - round0;
+  return left < 0 ? 0 : (left > kListCap ? kListCap : left);
+}
+
 // ---- element conversions ---------------------------------------------------------
 
 template <typename T> struct DT;

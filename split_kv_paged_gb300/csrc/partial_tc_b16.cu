@@ -13,7 +13,8 @@
 // P is sent as a 16-bit high part plus the 16-bit rounding of its remainder, so the product
 // carries about 16 significant bits of P (a bare bf16 P would round it to 8).
 //
-// Persistent CTAs, one per SM, take (request x kv head, split) items in turn; per item each
+// Persistent CTAs, one per SM, take the real (request x kv head, split) items of a work list
+// built on the device from the lengths, in turn (item k to CTA k mod grid); per item each
 // KV page of the split is read from HBM once (GQA packing: "split packed-Q8 verifier KV
 // scans", hipfire PR #760, Summary). Roles (256 threads):
 //   warp 0      K producer, warp 2 V producer: page ids one group of tiles ahead, one TMA box
@@ -65,7 +66,8 @@ constexpr uint32_t kOffX = kOffP + 2 * kPBuf;        // exchange: [2][4 warps][1
 constexpr uint32_t kOffBar = kOffX + 1024;
 constexpr uint32_t kNumBars = 4 * kStages + 4 * 2 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;   // + alignment slack
+constexpr uint32_t kOffList = kOffMisc + 64;            // work list + its scan scratch
+constexpr uint32_t kSmemBytes = kOffList + kListWords * 4 + 1024;   // + alignment slack
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPHalf % 1024 == 0, "operand alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -155,17 +157,23 @@ __global__ void __launch_bounds__(kThreads)
   for (uint32_t i = tid; i < 2 * kPBuf / 16; i += kThreads)
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sbase + kOffP + 16 * i), "r"(0));
   fence_proxy_async();
+  // The first work list is built while the TMEM allocation completes: its barriers also
+  // publish the TMEM address.
+  int* wlist = reinterpret_cast<int*>(sm + kOffList);
   tc_fence_before();
-  __syncthreads();
+  const int n_list0 = build_work_list(p, wlist, 0);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Bars bars{sbase + kOffBar};
   const uint32_t abort = sbase + kOffMisc + 4;
 
-  const int n_items = p.B * p.Hkv * p.num_splits;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-  const int u = item / p.num_splits, b = u / p.Hkv, g = u % p.Hkv, split = item % p.num_splits;
-  const int raw_ctx = p.context_lens[b];
+  // the real (request x kv head, split) items of the work list, in turn
+  int n_list = n_list0;
+  for (int round0 = 0;; round0 += kListCap) {
+  if (round0 > 0) n_list = build_work_list(p, wlist, round0);
+  for (int li = 0; li < n_list; li++) {
+  const int u = wlist[li] >> 8, b = u / p.Hkv, g = u % p.Hkv, split = wlist[li] & 255;
+  const int raw_ctx = wlist[kListCap + li];
   const int ctx = clamp_ctx(raw_ctx, p.max_ctx);
   if (raw_ctx != ctx && tid == 0 && split == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
   const Span sp = request_span(ctx, p.Lq, p.window, p.num_splits, p.min_chunk, p.align);
@@ -492,6 +500,8 @@ __global__ void __launch_bounds__(kThreads)
   tc_fence_before();
   __syncthreads();                         // item done: every copy, MMA and TMEM access drained
   if (ld_volatile_shared(abort)) break;
+  }
+  if (n_list < kListCap || (n_list > 0 && ld_volatile_shared(abort))) break;
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

@@ -2,9 +2,9 @@
 // scales, head_dim 128, up to 64 packed rows (Hq/Hkv query heads x Lq query rows) per KV
 // head, block size 8..128.
 //
-// Persistent CTAs, one per SM, take (request, kv head, split) items in turn (a split the
-// request does not use costs nothing but its span computation, so ragged batches launch no
-// idle CTAs). Per item, each KV page of the split is read from HBM once
+// Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
+// built on the device from the lengths, in turn (item k goes to CTA k mod grid, so a ragged
+// batch spreads its items over all CTAs). Per item, each KV page of the split is read from HBM once
 // (GQA packing: "split packed-Q8 verifier KV scans", hipfire PR #760, Summary). Roles:
 //   warp 0      K producer: walks the block table (read one group of tiles ahead) and
 //               TMA-loads each page's K slab (one 2-D box, 128-byte swizzle) into a 4-stage
@@ -86,7 +86,8 @@ constexpr uint32_t kOffJoint = kOffX + 2 * kXWg;
 constexpr uint32_t kOffBar = kOffJoint + 1280;
 constexpr uint32_t kNumBars = 4 * kStages + 2 + 2 + 2 + 2 + 2 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;        // + alignment slack
+constexpr uint32_t kOffList = kOffMisc + 64;                 // work list + its scan scratch
+constexpr uint32_t kSmemBytes = kOffList + kListWords * 4 + 1024;   // + alignment slack
 static_assert(kOffV % 1024 == 0 && kOffA % 1024 == 0, "stage alignment");
 static_assert(2 * 64 * 128 * 4 <= kStages * (kKStageBytes + kVStageBytes), "epilogue exchange B: K + V rings");
 static_assert(64 * 128 * 4 <= 32768, "epilogue exchange C: the Q area");
@@ -150,13 +151,15 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int* wlist = reinterpret_cast<int*>(sm + kOffList);
 
-  // Persistent: the CTAs (one per SM at most) stride over the (request x kv head, split) items;
-  // a split a request does not use costs one span computation. Each item runs its own
-  // pipeline from scratch (barriers re-initialised once the previous item has drained).
-  const int n_items = p.B * p.Hkv * p.num_splits;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-  const int u = item / p.num_splits, b = u / p.Hkv, g = u % p.Hkv, split = item % p.num_splits;
+  // Persistent: the CTAs (one per SM at most) take the real (request x kv head, split) items of
+  // the work list in turn. Each item runs its own pipeline from scratch (barriers re-initialised
+  // once the previous item has drained).
+  for (int round0 = 0;; round0 += kListCap) {
+  const int n_list = build_work_list(p, wlist, round0);
+  for (int li = 0; li < n_list; li++) {
+  const int u = wlist[li] >> 8, b = u / p.Hkv, g = u % p.Hkv, split = wlist[li] & 255;
   const int raw_ctx = p.context_lens[b];
   const int ctx = clamp_ctx(raw_ctx, p.max_ctx);
   if (raw_ctx != ctx && tid == 0 && split == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
@@ -419,14 +422,13 @@ __global__ void __launch_bounds__(kThreads)
     // pipeline (duty warps): tile wg in the ring, tile wg + 2 in registers, the page of tile
     // wg + 4 in flight
     int pgC = 0;
-    bool rdC = false, okB = false;
-    float ksB = 0.f, vsB = 0.f;
+    bool rdC = false, okA = false, okB = false;
+    float ksA = 0.f, vsA = 0.f, ksB = 0.f, vsB = 0.f;
     if (duty) {
       int pgA, pgB;
       const bool rdA = tok_page(wg, pgA), rdB = tok_page(wg + 2, pgB);
       rdC = tok_page(wg + 4, pgC);
-      float ksA, vsA;
-      const bool okA = tok_scales(wg, rdA, pgA, ksA, vsA);
+      okA = tok_scales(wg, rdA, pgA, ksA, vsA);
       okB = tok_scales(wg + 2, rdB, pgB, ksB, vsB);
       put(wg, ksA, vsA, okA);
     }
@@ -492,7 +494,8 @@ __global__ void __launch_bounds__(kThreads)
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.q_full());
-    } else {
+    }
+    if (wg == 1) {
       // warpgroup 1 reads the exponent once q_full (which the writer's warp arrives on after
       // the store) completes
       if (!mbar_wait(bars.q_full(), 0, abort)) set_abort(abort, p.status);
@@ -790,6 +793,8 @@ __global__ void __launch_bounds__(kThreads)
   // after a timed-out wait nothing more is started (copies may still be in flight); the
   // status word says the output is not valid
   if (ld_volatile_shared(abort)) break;
+  }
+  if (n_list < kListCap || (n_list > 0 && ld_volatile_shared(smem_u32(sm + kOffMisc + 4)))) break;
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

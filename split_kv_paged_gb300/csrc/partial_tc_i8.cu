@@ -8,7 +8,8 @@
 // the V scale the probability column). A bf16 Q row enters as f16 after a power-of-two scale
 // that is undone on the scores.
 //
-// Persistent CTAs, one per SM, take (request, kv head, split) items in turn; per item each KV
+// Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
+// built on the device from the lengths, in turn (item k to CTA k mod grid); per item each KV
 // page of the split is read from HBM once (GQA packing: "split packed-Q8 verifier KV scans",
 // hipfire PR #760, Summary). Roles:
 //   warp 0       producer: walks the block table one tile ahead and TMA-loads each page's int8
@@ -62,7 +63,8 @@ struct Lay {
   static constexpr uint32_t kOffMeta = kOffP + 128 * 128;     // P: 128 rows x 64 tokens f16
   static constexpr uint32_t kOffBar = kOffMeta + 4 * kMeta;   // meta ring: 4 tiles
   static constexpr uint32_t kOffMisc = kOffBar + 20 * 8;
-  static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;     // + alignment slack
+  static constexpr uint32_t kOffList = kOffMisc + 64;        // work list + its scan scratch
+  static constexpr uint32_t kSmem = kOffList + kListWords * 4 + 1024;   // + alignment slack
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(kStage16 % 1024 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0, "alignment");
   static_assert(4 * 32 * kEpiStride * 4 <= kStage16, "output staging fits in one f16 stage");
@@ -122,15 +124,18 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int* wlist = reinterpret_cast<int*>(sm + S::kOffList);
   const BarsI8 bars{sbase + S::kOffBar};
   const uint32_t abort = sbase + S::kOffMisc + 4;
   const int bs = p.bs, bs_sh = __ffs(bs) - 1;
   const int brows = bs < kT ? bs : kT;                     // rows of one TMA box
   const int ppt = bs < kT ? kT >> bs_sh : 1;               // pages a tile touches
 
-  const int n_items = p.B * p.Hkv * p.num_splits;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-  const int u = item / p.num_splits, b = u / p.Hkv, g = u % p.Hkv, split = item % p.num_splits;
+  // the real (request x kv head, split) items of the work list, in turn
+  for (int round0 = 0;; round0 += kListCap) {
+  const int n_list = build_work_list(p, wlist, round0);
+  for (int li = 0; li < n_list; li++) {
+  const int u = wlist[li] >> 8, b = u / p.Hkv, g = u % p.Hkv, split = wlist[li] & 255;
   const int raw_ctx = p.context_lens[b];
   const int ctx = clamp_ctx(raw_ctx, p.max_ctx);
   if (raw_ctx != ctx && tid == 0 && split == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
@@ -640,6 +645,8 @@ __global__ void __launch_bounds__(kThreads)
   tc_fence_before();
   __syncthreads();                                         // item done: every copy, MMA and TMEM access drained
   if (ld_volatile_shared(abort)) break;
+  }
+  if (n_list < kListCap || (n_list > 0 && ld_volatile_shared(abort))) break;
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);

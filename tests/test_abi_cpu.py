@@ -224,7 +224,7 @@ def test_tensor_core_kernels_reject_misaligned_pointers(lib, wl, field):
 
 @pytest.mark.parametrize("wl,S", [
     (W.mtp4_fp8_long(), 3),            # 600 items on 152 SMs: four even waves
-    (W.ragged_fp8(bs=128), 92),        # the 200k request spread over one wave
+    (W.ragged_fp8(bs=128), 131),       # 12-tile splits: 131 of the 200k request + 15 short, one wave
     (W.verify16_int8(), 36),
     (W.single_decode(), 8),
     (W.window_sink_bf16(), 1),         # HBM-bound 16-bit kernel: no split, no combine
@@ -274,3 +274,17 @@ def test_noalloc_checks_arguments_before_queueing_anything(lib):
         st = B.lib().tllm_decode_attn_splitkv_noalloc(q, 256, 256, 256, 256, wl.Lq, 256, None, 0, 2,
                                                       ctypes.byref(plan), 256, None)
         assert st == B.TLLM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bs", [128, 16])
+def test_planner_fits_the_ragged_batch_in_one_item_wave(lib, bs):
+    """The 200k + 15 x 1k batch: the work-based split size gives the long request as many
+    equal splits as leave one work-list item per SM, and each short request one split."""
+    wl = W.ragged_fp8(bs=bs)
+    plan = _plan(wl, host_ctx_lens=wl.ctx, num_sms=152)
+    counts = [B.tllm_decode_attn_split_range(plan, c, wl.Lq, 0, plan.num_splits, 0)[2] for c in wl.ctx]
+    assert sum(counts) * wl.Hkv <= 152
+    assert counts[1:] == [1] * 15
+    assert counts[0] == plan.num_splits > 92
+    sizes = [B.tllm_decode_attn_split_range(plan, wl.ctx[0], wl.Lq, 0, plan.num_splits, s) for s in range(counts[0])]
+    assert max(t1 - t0 for t0, t1, _ in sizes) == plan.min_chunk
