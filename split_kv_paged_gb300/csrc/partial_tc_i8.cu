@@ -11,23 +11,27 @@
 // Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
 // built on the device from the lengths, in turn (item k to CTA k mod grid); per item each KV
 // page of the split is read from HBM once (GQA packing: "split packed-Q8 verifier KV scans",
-// hipfire PR #760, Summary). Roles:
-//   warp 0       producer: walks the block table one tile ahead and TMA-loads each page's int8
-//                K and V rows (64-token tiles) into a 2-stage staging ring, with the tile's
-//                scales (cp.async) and page mask;
-//   warps 8..11  converters: widen a staged tile to f16 in the 128-byte-swizzle layout the
-//                MMAs read (rows = tokens, 64-element atoms), into a 2-stage ring, with the
-//                scales, the mask and the tile's largest V scale;
-//   warp 1       one thread issues every QK^T: A = Q in TMEM (written once per item), B = the
-//                f16 K tile (K-major), D = S in TMEM (two 64-column buffers);
-//   warp 3       one thread issues every PV: A = P in shared memory (K-major), B = the f16 V
-//                tile (MN-major, atoms 64 tokens x 128 B apart), D = O in TMEM;
-//   warps 4..7   softmax: thread = packed row (TMEM lane), so a row's maximum and sum never
-//                leave the thread. Online softmax in log2 units (tiny-llm PR #11: per-split
-//                online (m, l, acc)). P times the V scale is rounded once to f16 (2^-11
-//                relative), with a power-of-two factor 2^C that keeps it inside f16's range:
-//                C follows the largest V scale seen, only ever decreases, and O is then
-//                rescaled exactly.
+// hipfire PR #760, Summary). Roles (512 threads):
+//   warp 0        producer: walks the block table one tile ahead and TMA-loads each page's int8
+//                 K and V rows (64-token tiles) into a 3-stage staging ring, with the tile's
+//                 scales (cp.async) and page mask, so three tiles of HBM reads are in flight;
+//   warps 12..15  converters: widen a staged tile to f16 in the 128-byte-swizzle layout the
+//                 MMAs read (rows = tokens, 64-element atoms): warps 12, 13 the K half once the
+//                 previous tile's QK^T is done, warps 14, 15 the V half once the previous tile's
+//                 PV is done (one f16 stage); the tile's scales, page mask and largest V scale go
+//                 to a 4-slot meta ring;
+//   warp 1        one thread issues every QK^T: A = Q in TMEM (written once per item), B = the
+//                 f16 K tile (K-major), D = S in TMEM (two 64-column buffers);
+//   warp 3        one thread issues every PV: A = P in shared memory (K-major, two buffers),
+//                 B = the f16 V tile (MN-major, atoms 64 tokens x 128 B apart), D = O in TMEM;
+//   warps 4..11   softmax: two threads per packed row (TMEM lane), one per 32-token half of
+//                 the tile; they exchange their row maxima through shared memory, keep the same
+//                 running (maximum, P scale) and their own partial sums. Online softmax in log2
+//                 units (tiny-llm PR #11: per-split online (m, l, acc)). P times the V scale is
+//                 rounded once to f16 (2^-11 relative), with a power-of-two factor 2^C that keeps
+//                 it inside f16's range: C follows the largest V scale seen, only ever
+//                 decreases, and O is then rescaled exactly (each thread of a row its half of
+//                 the columns).
 //
 // Every wait is bounded in time; a timeout sets TLLM_FLAG_TIMEOUT, lets every role run to its
 // end without waiting, skips the output stores, takes no further item and frees TMEM.
@@ -44,11 +48,13 @@ namespace {
 using namespace ptx;
 
 constexpr int kT = 64;                 // tokens per tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr int kStages8 = 3;            // int8 staging ring depth
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;   // Q: D/2 columns, S: 2 x 64, O: D
 constexpr int kEpiStride = 36;          // floats per staged output row (32 + 4: conflict-free float4 rows)
+constexpr int kSmThreads = 256;         // softmax: 8 warps, two threads per TMEM lane
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
@@ -58,36 +64,39 @@ struct Lay {
   static constexpr uint32_t kSc = 2 * kT * 4;                 // K scales | V scales
   static constexpr uint32_t kMeta = kSc + 16;                 // scales | page mask | largest V scale x2
   static constexpr uint32_t kStage8 = align1k(2 * kT * D + kSc + 16);  // int8 K | V | scales | mask
-  static constexpr uint32_t kStage16 = 2 * kT * D * 2;                 // f16 K | f16 V
-  static constexpr uint32_t kOff8 = 0, kOff16 = 2 * kStage8, kOffP = kOff16 + 2 * kStage16;
-  static constexpr uint32_t kOffMeta = kOffP + 128 * 128;     // P: 128 rows x 64 tokens f16
-  static constexpr uint32_t kOffBar = kOffMeta + 4 * kMeta;   // meta ring: 4 tiles
-  static constexpr uint32_t kOffMisc = kOffBar + 20 * 8;
-  static constexpr uint32_t kOffList = kOffMisc + 64;        // work list + its scan scratch
+  static constexpr uint32_t kHalf16 = kT * D * 2;                      // one f16 tile (K or V)
+  static constexpr uint32_t kOff8 = 0, kOff16 = kStages8 * kStage8, kOffP = kOff16 + 2 * kHalf16;
+  static constexpr uint32_t kPBuf = 128 * 128;                // P: 128 rows x 64 tokens f16
+  static constexpr uint32_t kOffMeta = kOffP + 2 * kPBuf;     // meta ring: 4 tiles
+  static constexpr uint32_t kOffX = kOffMeta + 4 * kMeta;     // exchange floats (see xf below)
+  static constexpr uint32_t kOffBar = kOffX + 8 * 128 * 4;
+  static constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
+  static constexpr uint32_t kOffList = kOffMisc + 64;         // work list + its scan scratch
   static constexpr uint32_t kSmem = kOffList + kListWords * 4 + 1024;   // + alignment slack
   static_assert(kSmem <= 232448, "shared memory");
-  static_assert(kStage16 % 1024 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0, "alignment");
-  static_assert(4 * 32 * kEpiStride * 4 <= kStage16, "output staging fits in one f16 stage");
+  static_assert(kOff16 % 1024 == 0 && kOffP % 1024 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0, "alignment");
+  static_assert(8 * 32 * kEpiStride * 4 <= kStages8 * kStage8, "output staging fits in the int8 ring");
 };
 
-// mbarriers (8 bytes each), named by their shared-memory address. The f16 K and V halves of a
-// stage have their own barriers: K is free again once its QK^T is done, V once its PV is done,
-// so the converters widen K(j+1) while tile j's PV is still pending.
+// mbarriers (8 bytes each), named by their shared-memory address. The one f16 stage has a K
+// half and a V half with their own barriers: K is free again once its QK^T is done, V once its
+// PV is done, so the converters widen K(j+1) while tile j's PV is still pending.
 struct BarsI8 {
   uint32_t base;
   __device__ uint32_t at(uint32_t i) const { return base + 8u * i; }
   __device__ uint32_t full8(int s) const { return at(0 + s); }     // staged int8 tile landed
-  __device__ uint32_t empty8(int s) const { return at(2 + s); }    // converters done with it
-  __device__ uint32_t fullK(int s) const { return at(4 + s); }     // f16 K written (and the tile's meta)
-  __device__ uint32_t emptyK(int s) const { return at(6 + s); }    // its QK^T is done
-  __device__ uint32_t s_full(int s) const { return at(8 + s); }    // QK^T into S buffer s done
-  __device__ uint32_t s_free(int s) const { return at(10 + s); }   // S buffer s read
-  __device__ uint32_t p_full() const { return at(12); }            // P written, O rescaled
-  __device__ uint32_t pv_done() const { return at(13); }           // PV done
-  __device__ uint32_t q_full() const { return at(14); }            // Q in TMEM
-  __device__ uint32_t mma_fin() const { return at(15); }           // final commits of both issuers
-  __device__ uint32_t fullV(int s) const { return at(16 + s); }    // f16 V written
-  __device__ uint32_t emptyV(int s) const { return at(18 + s); }   // its PV is done
+  __device__ uint32_t empty8(int s) const { return at(3 + s); }    // converters done with it
+  __device__ uint32_t fullK() const { return at(6); }              // f16 K written
+  __device__ uint32_t emptyK() const { return at(7); }             // its QK^T is done
+  __device__ uint32_t fullV() const { return at(8); }              // f16 V written
+  __device__ uint32_t emptyV() const { return at(9); }             // its PV is done
+  __device__ uint32_t s_full(int s) const { return at(10 + s); }   // QK^T into S buffer s done
+  __device__ uint32_t s_free(int s) const { return at(12 + s); }   // S buffer s read
+  __device__ uint32_t p_full(int s) const { return at(14 + s); }   // P buffer s written (O rescaled)
+  __device__ uint32_t pv_done(int s) const { return at(16 + s); }  // PV from P buffer s done
+  __device__ uint32_t q_full() const { return at(18); }            // Q in TMEM
+  __device__ uint32_t mma_fin() const { return at(19); }           // final commits of both issuers
+  __device__ uint32_t meta_full(int s) const { return at(20 + s); }  // meta ring slot s written
 };
 
 __device__ __forceinline__ void set_abort_i8(uint32_t abort, uint32_t* status) {
@@ -130,6 +139,9 @@ __global__ void __launch_bounds__(kThreads)
   const int bs = p.bs, bs_sh = __ffs(bs) - 1;
   const int brows = bs < kT ? bs : kT;                     // rows of one TMA box
   const int ppt = bs < kT ? kT >> bs_sh : 1;               // pages a tile touches
+  // exchange floats of the two threads of a row: [0, 512) tile row maxima [parity][half][row],
+  // [512, 768) query maxima [half][row], [768, 1024) row sums [half][row]
+  float* xf = reinterpret_cast<float*>(sm + S::kOffX);
 
   // the real (request x kv head, split) items of the work list, in turn
   for (int round0 = 0;; round0 += kListCap) {
@@ -163,19 +175,22 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   if (tid == 0) {
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < kStages8; s++) {
       mbar_init(bars.full8(s), 1 + 32 + 1);                // expect_tx + 32 lanes' scale copies + mask
       mbar_init(bars.empty8(s), 4);                        // one elected lane per converter warp
-      mbar_init(bars.fullK(s), 4);                         // one elected lane per converter warp
-      mbar_init(bars.emptyK(s), 1);
-      mbar_init(bars.fullV(s), 4);
-      mbar_init(bars.emptyV(s), 1);
-      mbar_init(bars.s_full(s), 1);
-      mbar_init(bars.s_free(s), 4);                        // one elected lane per softmax warp
     }
-    mbar_init(bars.p_full(), 4);
-    mbar_init(bars.pv_done(), 1);
-    mbar_init(bars.q_full(), 4);
+    mbar_init(bars.fullK(), 2);                            // one elected lane per K converter warp
+    mbar_init(bars.emptyK(), 1);
+    mbar_init(bars.fullV(), 2);                            // one elected lane per V converter warp
+    mbar_init(bars.emptyV(), 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(bars.s_full(s), 1);
+      mbar_init(bars.s_free(s), 8);                        // one elected lane per softmax warp
+      mbar_init(bars.p_full(s), 8);
+      mbar_init(bars.pv_done(s), 1);
+    }
+    for (int s = 0; s < 4; s++) mbar_init(bars.meta_full(s), 4);
+    mbar_init(bars.q_full(), 8);
     mbar_init(bars.mma_fin(), 2);
     *reinterpret_cast<volatile int*>(sm + S::kOffMisc + 4) = 0;
     mbar_fence_init();
@@ -202,8 +217,8 @@ __global__ void __launch_bounds__(kThreads)
     int pg_next = page_of(0);
     int issued = 0;
     for (int j = 0; j < n_tiles; j++) {
-      const int st = j & 1;
-      if (j >= 2 && !mbar_wait(bars.empty8(st), ((j >> 1) - 1) & 1, abort)) set_abort_i8(abort, p.status);
+      const int st = j % kStages8;
+      if (j >= kStages8 && !mbar_wait(bars.empty8(st), ((j / kStages8) - 1) & 1, abort)) set_abort_i8(abort, p.status);
       if (ld_volatile_shared(abort)) break;
       const int pg = pg_next;
       pg_next = page_of(j + 1);
@@ -235,8 +250,8 @@ __global__ void __launch_bounds__(kThreads)
       issued = j + 1;
     }
     // drain: every issued stage's copies land before the item ends
-    for (int j = max(0, issued - 2); j < issued; j++)
-      if (!mbar_wait(bars.full8(j & 1), (j >> 1) & 1, 0u)) set_abort_i8(abort, p.status);
+    for (int j = max(0, issued - kStages8); j < issued; j++)
+      if (!mbar_wait(bars.full8(j % kStages8), (j / kStages8) & 1, 0u)) set_abort_i8(abort, p.status);
   } else if (warp == 1 || warp == 3) {
     // ---------------- MMA issuers: warp 1 every QK^T, warp 3 every PV (one thread each) ----------------
     if (lane == 0) {
@@ -244,33 +259,33 @@ __global__ void __launch_bounds__(kThreads)
       if (warp == 1) {
         const uint32_t idqk = idesc_f16(128, kT, 0, 0, 0);   // Q and K in f16
         ok = mbar_wait(bars.q_full(), 0, abort);
+        const uint32_t kt = sbase + S::kOff16;
         for (int j = 0; ok && j < n_tiles; j++) {
-          const int st = j & 1;
-          if (!mbar_wait(bars.fullK(st), (j >> 1) & 1, abort)) { ok = false; break; }
-          if (j >= 2 && !mbar_wait(bars.s_free(st), ((j >> 1) - 1) & 1, abort)) { ok = false; break; }
+          const int sb = j & 1;
+          if (!mbar_wait(bars.fullK(), j & 1, abort)) { ok = false; break; }
+          if (j >= 2 && !mbar_wait(bars.s_free(sb), ((j >> 1) - 1) & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sbase + S::kOff16 + st * S::kStage16;
 #pragma unroll
           for (int k = 0; k < D / 16; k++)
-            mma_f16_ts(tmem + kColS + 64 * st, tmem + kColQ + 8 * k,
+            mma_f16_ts(tmem + kColS + 64 * sb, tmem + kColQ + 8 * k,
                        sdesc_sw128(kt + (k >> 2) * S::kAtom + 32 * (k & 3), 16, 1024), idqk, k > 0 ? 1u : 0u);
-          mma_commit(bars.s_full(st));
-          mma_commit(bars.emptyK(st));
+          mma_commit(bars.s_full(sb));
+          mma_commit(bars.emptyK());
         }
       } else {
         const uint32_t idpv = idesc_f16(128, D, 0, 0, 1);   // P and V in f16
+        const uint32_t vt = sbase + S::kOff16 + S::kHalf16;
         for (int j = 0; ok && j < n_tiles; j++) {
-          const int st = j & 1;
-          if (!mbar_wait(bars.p_full(), j & 1, abort)) { ok = false; break; }
-          if (!mbar_wait(bars.fullV(st), (j >> 1) & 1, abort)) { ok = false; break; }
+          const int pb = j & 1;
+          if (!mbar_wait(bars.p_full(pb), (j >> 1) & 1, abort)) { ok = false; break; }
+          if (!mbar_wait(bars.fullV(), j & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t vt = sbase + S::kOff16 + st * S::kStage16 + kT * D * 2;
 #pragma unroll
           for (int k = 0; k < kT / 16; k++)
-            mma_f16_ss(tmem + kColO, sdesc_sw128(sbase + S::kOffP + 32 * k, 16, 1024),
+            mma_f16_ss(tmem + kColO, sdesc_sw128(sbase + S::kOffP + pb * S::kPBuf + 32 * k, 16, 1024),
                        sdesc_sw128(vt + 2048 * k, S::kAtom, 1024), idpv, (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(bars.pv_done());
-          mma_commit(bars.emptyV(st));
+          mma_commit(bars.pv_done(pb));
+          mma_commit(bars.emptyV());
         }
       }
       if (!ok) set_abort_i8(abort, p.status);
@@ -281,20 +296,25 @@ __global__ void __launch_bounds__(kThreads)
     // lanes 1..31 wait here for lane 0, so that the warp reaches the item's closing CTA barrier
     // (an aligned barrier) converged
     __syncwarp();
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------- converters: int8 tile -> f16 tile (exact), scales and mask ----------------
-    const int ct = tid - 256;                              // 0..127
+    // Warps 12, 13 widen K, warps 14, 15 widen V, each pair at its own pace: K(j + 1) waits only
+    // for the QK^T of tile j, V(j + 1) only for the PV of tile j.
+    const int ct = tid - 384;                              // 0..127
+    const int which = ct >> 6;                             // 0: K, 1: V
+    const int cw = ct & 63;                                // thread within the pair
     for (int j = 0; j < n_tiles; j++) {
-      const int st = j & 1;
-      if (!mbar_wait(bars.full8(st), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+      const int st = j % kStages8;
+      if (!mbar_wait(bars.full8(st), (j / kStages8) & 1, abort)) set_abort_i8(abort, p.status);
       const uint8_t* src = sm + S::kOff8 + st * S::kStage8;
-      const uint32_t dst = sbase + S::kOff16 + st * S::kStage16;
-      // The tile's meta first, into ring slot j % 4: scales (2 x kT floats), the page mask and
-      // the tile's largest |V scale| (warps 10, 11 hold the V scales; unread pages were
-      // zero-filled, and a non-finite scale is left out). The K scales leave here multiplied
-      // by the softmax scale in log2 units, so that a score reaches the softmax as one product
-      // with the query row's power of two, which is exact. Slot j % 4 last held tile j - 4,
-      // whose PV these threads already saw done (before widening tile j - 2's V).
+      const uint32_t dst = sbase + S::kOff16;
+      // The tile's meta first, into ring slot j % 4: scales (K by the K pair, V by the V pair),
+      // the page mask and the tile's largest |V scale| (unread pages were zero-filled, and a
+      // non-finite scale is left out). The K scales leave here multiplied by the softmax scale
+      // in log2 units, so that a score reaches the softmax as one product with the query row's
+      // power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax is over:
+      // tile j's copies were issued after both pairs released tile j - 3's stage, and the V pair
+      // widened tile j - 3 only after the PV of tile j - 4, which waited for that softmax.
       {
         const float scv = reinterpret_cast<const float*>(src + 2 * kT * D)[ct];
         uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
@@ -304,93 +324,94 @@ __global__ void __launch_bounds__(kThreads)
           *reinterpret_cast<uint32_t*>(meta + S::kSc) =
               *reinterpret_cast<const volatile uint32_t*>(src + 2 * kT * D + S::kSc);
         if (lane == 0 && ct >= kT) reinterpret_cast<float*>(meta + S::kSc + 4)[(ct - kT) >> 5] = vm;
-      }
-      // 16-element chunks (rows = tokens, atoms of 64 elements): K, released to QK^T (with the
-      // meta), then V, released to PV. Each thread loads all its chunks of one operand before
-      // converting any, so the loads overlap. int8 -> f16 exactly: the byte, sign bit flipped,
-      // placed under the f16 exponent of 1024 reads 1024 + (x + 128); subtracting 1152 leaves x.
-      constexpr int kChunksPerRow = D / 16, kPer = kT * kChunksPerRow / 128;
-      const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
-#pragma unroll
-      for (int which = 0; which < 2; which++) {
-        if (j >= 2 && !mbar_wait(which == 0 ? bars.emptyK(st) : bars.emptyV(st), ((j >> 1) - 1) & 1, abort))
-          set_abort_i8(abort, p.status);
-        uint4 w[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; i++) {
-          const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
-          w[i] = *reinterpret_cast<const uint4*>(src + which * kT * D + t * D + d0);
-        }
-#pragma unroll
-        for (int i = 0; i < kPer; i++) {
-          const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
-          const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
-                                  w[i].w ^ 0x80808080u};
-          uint32_t h[8];
-#pragma unroll
-          for (int e = 0; e < 8; e++) {
-            const uint32_t x = __byte_perm(ws[e >> 1], 0x64646464u, (e & 1) ? 0x5342u : 0x5140u);
-            const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-            h[e] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
-          const uint32_t base = dst + which * kT * D * 2 + (d0 >> 6) * S::kAtom;
-          const uint32_t byte = (d0 & 63) * 2;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
-                       "r"(h[2]), "r"(h[3]));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
-                       "r"(h[5]), "r"(h[6]), "r"(h[7]));
-        }
-        fence_proxy_async();
         __syncwarp();
-        if (lane == 0) {
-          if (which == 0) {
-            mbar_arrive(bars.fullK(st));
-          } else {
-            mbar_arrive(bars.empty8(st));
-            mbar_arrive(bars.fullV(st));
-          }
+        if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
+      }
+      // 16-element chunks (rows = tokens, atoms of 64 elements). Each thread loads all its
+      // chunks before converting any, so the loads overlap. int8 -> f16 exactly: the byte, sign
+      // bit flipped, placed under the f16 exponent of 1024 reads 1024 + (x + 128); subtracting
+      // 1152 leaves x.
+      constexpr int kChunksPerRow = D / 16, kPer = kT * kChunksPerRow / 64;
+      const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
+      // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
+      if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
+        set_abort_i8(abort, p.status);
+      uint4 w[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; i++) {
+        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
+        w[i] = *reinterpret_cast<const uint4*>(src + which * kT * D + t * D + d0);
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; i++) {
+        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
+        const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
+                                w[i].w ^ 0x80808080u};
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+          const uint32_t x = __byte_perm(ws[e >> 1], 0x64646464u, (e & 1) ? 0x5342u : 0x5140u);
+          const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+          h[e] = *reinterpret_cast<const uint32_t*>(&v2);
         }
+        const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
+        const uint32_t byte = (d0 & 63) * 2;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
+                     "r"(h[2]), "r"(h[3]));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
+                     "r"(h[5]), "r"(h[6]), "r"(h[7]));
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(which == 0 ? bars.fullK() : bars.fullV());
+        mbar_arrive(bars.empty8(st));
       }
     }
-    // the releases of the last two f16 stages by their MMAs (asynchronous tcgen05.commit
-    // arrivals) must have landed before the next item re-initialises the barriers
-    for (int j = max(0, n_tiles - 2); j < n_tiles; j++) {
-      if (!mbar_wait(bars.emptyK(j & 1), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
-      if (!mbar_wait(bars.emptyV(j & 1), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
-    }
+    // the release of the f16 stage by the last tile's MMA (an asynchronous tcgen05.commit
+    // arrival) must have landed before the next item re-initialises the barriers
+    if (!mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (n_tiles - 1) & 1, abort))
+      set_abort_i8(abort, p.status);
   } else if (warp >= 4) {
-    // ---------------- softmax: thread = packed row r (TMEM lane) ----------------
+    // ---------------- softmax: two threads per packed row r (TMEM lane), one per token half ----------------
+    const int hh = (warp - 4) >> 2;                        // token half (0: tokens 0..31, 1: 32..63)
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const bool real = r < p.R;
     const int qi = real ? r / p.G : 0, qh = g * p.G + (real ? r % p.G : 0);
     const int pos = real ? ctx - p.Lq + qi : -1;
-    // Q row -> TMEM columns [0, D/2) in f16, two elements per column (even element low). A bf16
-    // row is first scaled by 2^e so that its largest |q| lies in [2^13, 2^14): every element
-    // that is at least 2^-14 after scaling converts exactly (bf16 carries 8 significant bits,
-    // f16 11); a smaller one rounds by at most 2^-25, far below the fp32 rounding of a score
-    // whose largest term is near 2^13 |k|. The scores are scaled back by qscale = 2^-e, a
-    // power of two, so the row maximum in log2 units is exact and the largest term of every
-    // row's exponent sum is exactly 2^C, however large the scores.
+    // Q row -> TMEM columns [0, D/2) in f16, two elements per column (even element low); this
+    // thread converts elements [hh D/2, (hh + 1) D/2). A bf16 row is first scaled by 2^e so that
+    // its largest |q| lies in [2^13, 2^14): every element that is at least 2^-14 after scaling
+    // converts exactly (bf16 carries 8 significant bits, f16 11); a smaller one rounds by at most
+    // 2^-25, far below the fp32 rounding of a score whose largest term is near 2^13 |k|. The
+    // scores are scaled back by qscale = 2^-e, a power of two, so the row maximum in log2 units
+    // is exact and the largest term of every row's exponent sum is exactly 2^C, however large
+    // the scores.
     float qscale = 1.f;
     {
       const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                         ((int64_t)(b * p.Lq + qi) * p.Hq + qh) * D);
+                                                         ((int64_t)(b * p.Lq + qi) * p.Hq + qh) * D + hh * (D / 2));
       const bool qbf = p.q_dtype == TLLM_BF16;
-      // the whole row is loaded at once (one memory round trip; it is on the path to the first QK^T)
-      uint4 qv[D / 8];
+      // the thread's half row is loaded at once (one memory round trip; it is on the path to
+      // the first QK^T)
+      uint4 qv[D / 16];
 #pragma unroll
-      for (int c = 0; c < D / 8; c++) qv[c] = real ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < D / 16; c++) qv[c] = real ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
       float emul = 1.f;
       if (qbf) {
         float mx = 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 8; c++) {
+        for (int c = 0; c < D / 16; c++) {
           const uint32_t xs[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
 #pragma unroll
           for (int k = 0; k < 4; k++)
             mx = fmax3(mx, fabsf(__uint_as_float(xs[k] << 16)), fabsf(__uint_as_float(xs[k] & 0xffff0000u)));
         }
+        // the row's largest |q| over both halves
+        xf[512 + 128 * hh + r] = mx;
+        named_bar(1, kSmThreads);
+        mx = fmaxf(xf[512 + r], xf[640 + r]);
         int e = 0;
         if (mx > 0.f && mx <= 3.402823466e38f) {
           int ex;
@@ -401,7 +422,7 @@ __global__ void __launch_bounds__(kThreads)
         qscale = __int_as_float((127 - e) << 23);
       }
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+      for (int c0 = 0; c0 < D / 4; c0 += 32) {
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; c++) {
@@ -419,36 +440,36 @@ __global__ void __launch_bounds__(kThreads)
             w[k] = *reinterpret_cast<const uint32_t*>(&h2);
           }
         }
-        tmem_st32(tmem + lane_off + kColQ + c0, w);
+        tmem_st32(tmem + lane_off + kColQ + hh * (D / 4) + c0, w);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.q_full());
     }
-    float M = -INFINITY, l = 0.f;                          // running max (log2 units), sum (units of 2^-C)
+    float M = -INFINITY, l = 0.f;                          // running max (log2 units), this half's sum (units of 2^-C)
     int C = 1 << 20;                                       // P scale exponent, unset
     float e0_run = 0.f;                                    // exponent offset of O and l
     int last = -1;
     for (int j = 0; j < n_tiles; j++) {
       last = j;
-      const int st = j & 1;
+      const int sb = j & 1;
       const int tt = t0 + j * kT;
       const uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
-      const float* ksc = reinterpret_cast<const float*>(meta);
-      const float* vsc = ksc + kT;
-      if (!mbar_wait(bars.fullK(st), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+      const float* ksc = reinterpret_cast<const float*>(meta) + 32 * hh;
+      const float* vsc = reinterpret_cast<const float*>(meta) + kT + 32 * hh;
+      if (!mbar_wait(bars.meta_full(j & 3), (j >> 2) & 1, abort)) set_abort_i8(abort, p.status);
       const uint32_t pmask = *reinterpret_cast<const volatile uint32_t*>(meta + S::kSc);
       const float vmax = fmaxf(reinterpret_cast<const float*>(meta + S::kSc + 4)[0],
                                reinterpret_cast<const float*>(meta + S::kSc + 4)[1]);
-      if (!mbar_wait(bars.s_full(st), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+      if (!mbar_wait(bars.s_full(sb), (j >> 1) & 1, abort)) set_abort_i8(abort, p.status);
       tc_fence_after();
-      uint32_t sreg[64];
-      tmem_ld64(tmem + lane_off + kColS + 64 * st, sreg);
-      tmem_ld_wait();
+      uint32_t sreg[32];
+      tmem_ld32(tmem + lane_off + kColS + 64 * sb + 32 * hh, sreg);
+      tmem_ld_wait(sreg);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.s_free(st));
+      if (lane == 0) mbar_arrive(bars.s_free(sb));
 
       // scores: u = raw x K scale (masked tokens -inf; their scales may be anything, NaN
       // included, so masking selects rather than multiplies). A tile every row sees whole (all
@@ -459,10 +480,10 @@ __global__ void __launch_bounds__(kThreads)
       const uint32_t full_pages = ppt >= 32 ? kFull : ((1u << ppt) - 1u);
       const bool whole = pmask == full_pages && tt >= vlo && tt + kT <= t1 && tt + kT - 1 <= ctx - p.Lq &&
                          (p.window <= 0 || tt > ctx - 1 - p.window);
-      float u[64];
+      float u[32];
       if (whole) {
 #pragma unroll
-        for (int i4 = 0; i4 < 16; i4++) {
+        for (int i4 = 0; i4 < 8; i4++) {
           const float4 k4 = ks4[i4];
           const float2 a = fmul2(make_float2(__uint_as_float(sreg[4 * i4]), __uint_as_float(sreg[4 * i4 + 1])),
                                  make_float2(k4.x, k4.y));
@@ -475,9 +496,9 @@ __global__ void __launch_bounds__(kThreads)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; i++) {
-          const int t = tt + i;
-          const int slot = bs < kT ? i >> bs_sh : 0;
+        for (int i = 0; i < 32; i++) {
+          const int ti = 32 * hh + i, t = tt + ti;
+          const int slot = bs < kT ? ti >> bs_sh : 0;
           const bool vis = ((pmask >> slot) & 1) && t >= vlo && t < t1 && t <= pos &&
                            (p.window <= 0 || pos - t < p.window);
           u[i] = vis ? __uint_as_float(sreg[i]) * ksc[i] : -INFINITY;
@@ -486,12 +507,17 @@ __global__ void __launch_bounds__(kThreads)
       // rows past R see nothing (their scores stay -inf)
       if (!real) {
 #pragma unroll
-        for (int i = 0; i < 64; i++) u[i] = -INFINITY;
+        for (int i = 0; i < 32; i++) u[i] = -INFINITY;
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < 32; k++) m4[k & 3] = fmax3(m4[k & 3], u[2 * k], u[2 * k + 1]);
-      const float mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      for (int k = 0; k < 16; k++) m4[k & 3] = fmax3(m4[k & 3], u[2 * k], u[2 * k + 1]);
+      // the row maximum over both halves (slot by tile parity: the partner may still be reading
+      // the previous tile's)
+      float* xm = xf + 256 * sb;
+      xm[128 * hh + r] = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      named_bar(1, kSmThreads);
+      const float mx = fmaxf(xm[r], xm[128 + r]);
       // P scale exponent C: vmax * 2^C < 2^14; it only ever decreases (then O is rescaled)
       if (vmax > 0.f) {
         int ex;
@@ -503,15 +529,16 @@ __global__ void __launch_bounds__(kThreads)
       // p' = 2^(u qscale + e0) with e0 = C - M (rounded): the row's largest term is 2^C. O and l
       // are kept in units of 2^-e0 for the e0 actually used, so its rounding cancels in O / l
       // and in the LSE (log2 l - e0), and a change of e0 rescales both by 2^(e0 - e0_prev).
+      // Both threads of a row hold the same M, C and e0.
       const float M_new = fmaxf(M, mx * qscale);
       const float e0 = M_new == -INFINITY ? 0.f : (float)C - M_new;
       const float factor = M == -INFINITY ? (M_new == -INFINITY ? 1.f : 0.f) : ex2f(e0 - e0_run);
       e0_run = e0;
       const float2 qs2 = make_float2(qscale, qscale), e02 = make_float2(e0, e0);
       float2 ls = make_float2(0.f, 0.f);
-      uint32_t pw[32];
+      uint32_t pw[16];
 #pragma unroll
-      for (int i4 = 0; i4 < 16; i4++) {
+      for (int i4 = 0; i4 < 8; i4++) {
         const float4 v = vs4[i4];
         const float2 x01 = ffma2(make_float2(u[4 * i4], u[4 * i4 + 1]), qs2, e02);
         const float2 x23 = ffma2(make_float2(u[4 * i4 + 2], u[4 * i4 + 3]), qs2, e02);
@@ -529,60 +556,68 @@ __global__ void __launch_bounds__(kThreads)
       const float prev_M = M;
       M = M_new;
 
-      // the P buffer and O are free once the previous PV is done
-      if (j >= 1 && !mbar_wait(bars.pv_done(), (j - 1) & 1, abort)) set_abort_i8(abort, p.status);
-      const uint32_t prow = sbase + S::kOffP;
+      // P buffer sb is free once the PV of tile j - 2 (which read it) is done
+      if (j >= 2 && !mbar_wait(bars.pv_done(sb), ((j - 2) >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+      const uint32_t prow = sbase + S::kOffP + sb * S::kPBuf;
 #pragma unroll
-      for (int c = 0; c < 8; c++)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + swz(r, 16 * c)), "r"(pw[4 * c]),
-                     "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3]));
+      for (int c = 0; c < 4; c++)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + swz(r, 64 * hh + 16 * c)),
+                     "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3]));
       fence_proxy_async();
-      // rescale this row of O when its maximum grew or the P scale shrank (O holds tiles < j)
+      // rescale this row of O (this thread: half of its columns) when its maximum grew or the P
+      // scale shrank: O holds the tiles < j, so the PV of tile j - 1 must be done first
       const bool need = j >= 1 && factor != 1.f && prev_M != -INFINITY;
       if (__any_sync(kFull, need)) {
+        if (!mbar_wait(bars.pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort)) set_abort_i8(abort, p.status);
         tc_fence_after();
         const float f = need ? factor : 1.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kColO + c0, o);
+          tmem_ld32(tmem + lane_off + kColO + hh * (D / 2) + c0, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tmem + lane_off + kColO + c0, o);
+          tmem_st32(tmem + lane_off + kColO + hh * (D / 2) + c0, o);
         }
         tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full());
+      if (lane == 0) mbar_arrive(bars.p_full(sb));
     }
 
     // ---------------- epilogue: O / l (record or final output) ----------------
-    if (last >= 0 && !mbar_wait(bars.pv_done(), last & 1, abort)) set_abort_i8(abort, p.status);
+    // the last two PVs (one per P buffer): each commit's arrival lands before the item ends
+    if (last >= 1 && !mbar_wait(bars.pv_done((last - 1) & 1), ((last - 1) >> 1) & 1, abort))
+      set_abort_i8(abort, p.status);
+    if (last >= 0 && !mbar_wait(bars.pv_done(last & 1), (last >> 1) & 1, abort)) set_abort_i8(abort, p.status);
     tc_fence_after();
+    xf[768 + 128 * hh + r] = l;
+    named_bar(1, kSmThreads);
+    const float lt = xf[768 + r] + xf[896 + r];
     // (the TMEM loads are warp-collective: every lane takes part, only real rows store)
     const bool store = real && !ld_volatile_shared(abort);
     float mul = 0.f;
     // O and l are both in units of 2^-e0
     if (finalize) {
-      if (l > 0.f) mul = 1.f / (l + (p.sinks ? ex2f(p.sinks[qh] * kLog2e + e0_run) : 0.f));
+      if (lt > 0.f) mul = 1.f / (lt + (p.sinks ? ex2f(p.sinks[qh] * kLog2e + e0_run) : 0.f));
     } else {
-      mul = l > 0.f ? 1.f / l : 0.f;
-      if (store) p.ws_lse[(int64_t)u_split * p.R + r] = l > 0.f ? log2f(l) - e0_run : -INFINITY;
+      mul = lt > 0.f ? 1.f / lt : 0.f;
+      if (store && hh == 0) p.ws_lse[(int64_t)u_split * p.R + r] = lt > 0.f ? log2f(lt) - e0_run : -INFINITY;
     }
     // O leaves through shared memory, 32 columns at a time: a thread holds one row, so storing
     // from registers would touch 32 rows per instruction; staged, each warp stores its own 32
-    // rows as whole 128-byte lines. The f16 stage 0 is free here: every QK^T of the item
-    // finished before its scores were read, every PV before pv_done, and the converters are done.
-    float* stage = reinterpret_cast<float*>(sm + S::kOff16) + (warp & 3) * 32 * kEpiStride;
+    // rows as whole 128-byte lines. The int8 staging ring is free here: every tile's copies
+    // landed and were widened before its PV.
+    float* stage = reinterpret_cast<float*>(sm + S::kOff8) + (warp - 4) * 32 * kEpiStride;
     const bool keep = !ld_volatile_shared(abort);
     // output row offset of this lane's row (-1: padding), computed once and shuffled to the
     // lanes that store it
     int64_t out_row = -1;
     if (r < p.R) out_row = ((int64_t)(b * p.Lq + r / p.G) * p.Hq + g * p.G + r % p.G) * D;
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = hh * (D / 2); c0 < (hh + 1) * (D / 2); c0 += 32) {
       uint32_t o[32];
       tmem_ld32(tmem + lane_off + kColO + c0, o);
       tmem_ld_wait();
