@@ -35,9 +35,12 @@
  *   q            [B, Lq, Hq, D]            q_dtype (f16, bf16 or f32)
  *   out          [B, Lq, Hq, D]            out_dtype (f16, bf16 or f32)
  *   k_cache      [num_pages, Hkv, bs, D]   kv_dtype (f16, bf16, fp8 e4m3 or int8)
- *   v_cache      [num_pages, Hkv, bs, D]   kv_dtype
+ *   v_cache      [num_pages, Hkv, bs, D]   kv_dtype ([num_pages, Hkv, D, bs] with TLLM_V_DIM_MAJOR)
  *   kv_scales    [2, num_pages, Hkv, bs]   fp32: K scales then V scales (quantised KV only, else NULL)
- *   block_table  [B, max_blocks_per_seq]   int32 physical page ids
+ *   block_table  [B, max_blocks_per_seq]   int32 physical page ids, or NULL for a contiguous
+ *                                          cache: block i of request b is then page
+ *                                          b * max_blocks_per_seq + i (tiny-llm PR #11, design
+ *                                          section: the ContiguousRows address mode)
  *   context_lens [B]                       int32 KV length INCLUDING the Lq new rows;
  *                                          row i sits at position ctx - Lq + i
  *   sinks        [Hq]                      fp32 sink logit per query head, or NULL
@@ -82,6 +85,14 @@ typedef enum {
   TLLM_KERNEL_TC_B16 = 5             /* tcgen05 16-bit kernel, f16 / bf16 KV and Q, head_dim 128, <= 16 rows */
 } tllm_kernel;
 
+/* Layout of v_cache within a page (aiter PR #5628, Performance table: plain and "transposed"
+ * V). K always uses the token-major layout. */
+typedef enum {
+  TLLM_V_TOKEN_MAJOR = 0,            /* v_cache [num_pages, Hkv, bs, D]: a token's D values contiguous */
+  TLLM_V_DIM_MAJOR = 1               /* v_cache [num_pages, Hkv, D, bs]: each dimension's bs values contiguous
+                                        (the transposed V cache) */
+} tllm_v_layout;
+
 /* Device status bits written into the workspace header. */
 #define TLLM_FLAG_CTX_CLAMPED   0x1u  /* some context_lens[b] was < 0 or > max_blocks*bs; clamped */
 #define TLLM_FLAG_BAD_PAGE      0x2u  /* some referenced page id was outside [0, num_pages); masked */
@@ -98,6 +109,7 @@ typedef struct {
   tllm_dtype q_dtype, kv_dtype, out_dtype;
   float softmax_scale;               /* 0 => 1/sqrt(head_dim) */
   tllm_kernel kernel;                /* TLLM_KERNEL_AUTO unless a test pins a variant */
+  tllm_v_layout v_layout;            /* TLLM_V_TOKEN_MAJOR unless the V cache is transposed */
 } tllm_decode_attn_desc;
 
 /* Host POD produced by tllm_decode_attn_plan; copy it freely. */
@@ -155,7 +167,8 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
  * flash-decoding combine, device-side lengths, zero allocation during capture).
  *   q, k_cache, v_cache, block_table, context_lens, kv_scales, sinks, out: device
  *     pointers in the layouts above (kv_scales required for FP8/INT8 KV, ignored
- *     otherwise; sinks may be NULL). The tensor-core kernels also need q, k_cache,
+ *     otherwise; sinks may be NULL; block_table may be NULL for a contiguous cache, which
+ *     then needs num_pages >= batch * max_blocks_per_seq). The tensor-core kernels also need q, k_cache,
  *     v_cache and kv_scales 16-byte aligned (TMA boxes, 16-byte query loads), and the
  *     FP8 and INT8 ones `out` too (16-byte row stores); a misaligned pointer returns
  *     TLLM_ERR_INVALID_ARG.

@@ -30,6 +30,7 @@ tllm_status check_desc(const tllm_decode_attn_desc* d) {
   if (!q_ok(d->q_dtype) || !kv_ok(d->kv_dtype) || !q_ok(d->out_dtype)) return TLLM_ERR_UNSUPPORTED;
   if (d->block_size > 256) return TLLM_ERR_UNSUPPORTED;
   if (d->kernel < TLLM_KERNEL_AUTO || d->kernel > TLLM_KERNEL_TC_B16) return TLLM_ERR_INVALID_ARG;
+  if (d->v_layout != TLLM_V_TOKEN_MAJOR && d->v_layout != TLLM_V_DIM_MAJOR) return TLLM_ERR_INVALID_ARG;
   return TLLM_OK;
 }
 
@@ -327,7 +328,9 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   tllm_status st = check_desc(&pl.desc);
   if (st != TLLM_OK) return st;
   const tllm_decode_attn_desc& d = pl.desc;
-  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out) return TLLM_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !context_lens || !out) return TLLM_ERR_INVALID_ARG;
+  // no block table: a contiguous cache, request b's block i at page b * max_blocks_per_seq + i
+  if (!block_table && (int64_t)pl.batch * d.max_blocks_per_seq > d.num_pages) return TLLM_ERR_INVALID_ARG;
   if (quantised(d.kv_dtype) && !kv_scales) return TLLM_ERR_INVALID_ARG;
   if (query_len <= 0 || query_len > pl.query_len || window < 0) return TLLM_ERR_INVALID_ARG;
   if (num_splits <= 0 || num_splits > pl.max_splits) return TLLM_ERR_INVALID_ARG;
@@ -374,6 +377,7 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->q_dtype = d.q_dtype;
   p->kv_dtype = d.kv_dtype;
   p->out_dtype = d.out_dtype;
+  p->v_dim_major = d.v_layout == TLLM_V_DIM_MAJOR;
   // alignment the chosen kernel's copies need (TMA boxes, 16-byte loads and stores)
   bool aligned = true;
   switch (pl.kernel) {

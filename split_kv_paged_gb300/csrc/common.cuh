@@ -22,7 +22,7 @@ struct Params {
   const void* q;
   const void* k_cache;
   const void* v_cache;
-  const int32_t* block_table;
+  const int32_t* block_table;       // [B, max_blocks] or nullptr (contiguous cache)
   const int32_t* context_lens;
   const float* k_scales;            // [num_pages, Hkv, bs] or nullptr
   const float* v_scales;
@@ -36,6 +36,7 @@ struct Params {
   int max_ctx;                      // max_blocks * bs: lengths are clamped to it
   float scale_log2;                 // softmax scale * log2(e)
   int q_dtype, kv_dtype, out_dtype;
+  int v_dim_major;                  // v_cache [num_pages, Hkv, D, bs] (TLLM_V_DIM_MAJOR)
 };
 
 // ---- the split rule (host and device) -------------------------------------------
@@ -77,6 +78,15 @@ TLLM_HD Span request_span(int ctx, int Lq, int window, int num_splits, int min_c
   int n = (vis + c - 1) / c;
   s.nsplit = n < 1 ? 1 : n;
   return s;
+}
+
+// ---- page lookup ----------------------------------------------------------------------
+// Physical page of block `blk` of request b: the block table's entry, or, for a contiguous
+// cache (no block table: "split-KV decode attention design record", tiny-llm PR #11, design
+// section, the ContiguousRows address mode), block blk of request b is page
+// b * max_blocks + blk, so the cache is [batch][max_blocks][Hkv][bs][D] in one piece.
+__device__ __forceinline__ int page_at(const Params& p, int b, int blk) {
+  return p.block_table ? __ldg(p.block_table + (int64_t)b * p.max_blocks + blk) : b * p.max_blocks + blk;
 }
 
 // ---- the work list of the persistent partial kernels ----------------------------------

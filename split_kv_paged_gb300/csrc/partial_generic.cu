@@ -2,6 +2,8 @@
 // head_dim 64/128/256, any block size. It is the correctness baseline every faster
 // variant is compared with, and the fallback for shapes they do not cover.
 //
+// It also reads a dimension-major ("transposed") V cache, [num_pages, Hkv, D, bs].
+//
 // One CTA = one (request, kv head, split, block of 16 packed rows). The packed rows of
 // a KV head are its G query heads times the Lq query rows (GQA packing: "split packed-Q8
 // verifier KV scans", hipfire PR #760, Summary). The CTA walks its split's tokens in
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) partial_generic_kernel(Params p) {
       int64_t row = -1;
       float ks = 0.f, vs = 0.f;
       if (t >= sp.lo && t < t1) {                      // keys below the window are never read
-        int page = p.block_table[(int64_t)b * p.max_blocks + t / p.bs];
+        int page = page_at(p, b, t / p.bs);
         if (page < 0 || page >= p.num_pages) {
           atomicOr(p.status, TLLM_FLAG_BAD_PAGE);
         } else {
@@ -97,7 +99,10 @@ __global__ void __launch_bounds__(kThreads) partial_generic_kernel(Params p) {
       float kv = 0.f, vv = 0.f;
       if (row >= 0) {
         kv = to_f32(kc[row * D + d]);
-        vv = to_f32(vc[row * D + d]);
+        // row = (page * Hkv + g) * bs + slot; a dimension-major V page keeps each
+        // dimension's bs values together
+        const int64_t slot = row % p.bs;
+        vv = to_f32(vc[p.v_dim_major ? (row - slot) * D + (int64_t)d * p.bs + slot : row * D + d]);
       }
       k_s[j * (D + 1) + d] = kv;
       v_s[j * D + d] = vv;

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
   auto page_of = [&](int jt, int i) -> int {
     const int first = t0 + jt * kTile + i * bs;         // first token of the slot
     if (jt >= n_tiles || first >= t1 || first + bs <= vlo) return -1;
-    const int pg = p.block_table[(int64_t)b * p.max_blocks + (first >> bs_sh)];
+    const int pg = page_at(p, b, first >> bs_sh);
     if (pg < 0 || pg >= p.num_pages) {
       atomicOr(p.status, TLLM_FLAG_BAD_PAGE);
       return -1;
@@ -462,7 +462,8 @@ bool simt_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   const bool kv_ok = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16 || d.kv_dtype == TLLM_FP8_E4M3 ||
                      d.kv_dtype == TLLM_INT8;
-  return kv_ok && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) && rows >= 1 && rows <= 8 &&
+  return kv_ok && d.v_layout == TLLM_V_TOKEN_MAJOR && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) &&
+         rows >= 1 && rows <= 8 &&
          (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128);
 }
 

@@ -202,7 +202,6 @@ __global__ void __launch_bounds__(kThreads)
   const int bs_sh = __ffs(bs) - 1;                   // bs is a power of two, 8..128
   const int ppt_sh = 7 - bs_sh, ppt = 1 << ppt_sh;   // pages per tile (1..16)
   const int gt_sh = 5 - ppt_sh, gt = 1 << gt_sh;     // tiles per group of 32 page ids
-  const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
   // page ids of a group of tiles, one per lane (lane = tile of the group x page slot)
   auto fetch = [&](int grp, int& pg, int& need) {
     const int tile = (grp << gt_sh) + (lane >> ppt_sh), slot = lane & (ppt - 1);
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(kThreads)
       const int tt = t0 + tile * kTile, first = tt + slot * bs;
       if (max(first, sp.lo) < min(first + bs, t1)) {
         need = 1;
-        pg = bt[(tt >> bs_sh) + slot];
+        pg = page_at(p, b, (tt >> bs_sh) + slot);
       }
     }
   };
@@ -376,7 +375,7 @@ __global__ void __launch_bounds__(kThreads)
     // this thread's token of tile jt: its page id, or -1 when the split does not read it
     auto tok_page = [&](int jt) -> int {
       const int t = t0 + jt * kTile + L;
-      return (jt < n_tiles && t >= sp.lo && t < t1) ? __ldg(bt + (t >> bs_sh)) : -1;
+      return (jt < n_tiles && t >= sp.lo && t < t1) ? page_at(p, b, t >> bs_sh) : -1;
     };
     int pg_tok = tok_page(0);
     const int last = n_tiles - 1;
@@ -558,6 +557,7 @@ cudaError_t launch_bf(const Params& p, const CUtensorMap& km, const CUtensorMap&
 bool tc_b16_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   return (d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16) && d.q_dtype == d.kv_dtype && d.head_dim == kD &&
+         d.v_layout == TLLM_V_TOKEN_MAJOR &&
          rows >= 1 && rows <= kNq && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
 }

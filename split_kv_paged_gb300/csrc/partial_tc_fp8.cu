@@ -137,6 +137,9 @@ __device__ __forceinline__ void set_abort(uint32_t abort, uint32_t* status) {
   }
 }
 
+// kVdm: the V cache is dimension-major ([pages, Hkv, D, bs]); a separate instance, so the
+// token-major one is compiled exactly as without it
+template <bool kVdm>
 __global__ void __launch_bounds__(kThreads)
     partial_tc_fp8_kernel(const Params p, const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap) {
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kThreads)
       const int tt = t0 + tile * kTile, first = tt + slot * bs;
       if (max(first, sp.lo) < min(first + bs, t1)) {
         need = 1;
-        pg = p.block_table[(int64_t)b * p.max_blocks + (tt >> bs_sh) + slot];
+        pg = page_at(p, b, (tt >> bs_sh) + slot);
       }
     }
   };
@@ -302,8 +305,17 @@ __global__ void __launch_bounds__(kThreads)
       if (page >= 0) {
         const int64_t row = ((int64_t)page * p.Hkv + g) * bs;
         const int st = jl % kStages;
-        if (isk) tma_load_2d(sbase + st * kKStageBytes + slot * bs * kD, &kmap, 0, (int)row, full + 8 * (st));
-        else tma_load_2d(sbase + kOffV + st * kVStageBytes + slot * bs * kD, &vmap, 0, (int)row, full + 8 * (st));
+        if (isk) {
+          tma_load_2d(sbase + st * kKStageBytes + slot * bs * kD, &kmap, 0, (int)row, full + 8 * (st));
+        } else if constexpr (!kVdm) {
+          tma_load_2d(sbase + kOffV + st * kVStageBytes + slot * bs * kD, &vmap, 0, (int)row, full + 8 * (st));
+        } else {
+          // dimension-major V page: bs / 16 boxes of 128 dims x 16 tokens, each a 2 KB block of
+          // core matrices; block k of the tile holds its tokens 16 k .. 16 k + 15
+          for (int c = 0; c < (bs >> 4); c++)
+            tma_load_2d(sbase + kOffV + st * kVStageBytes + (slot * (bs >> 4) + c) * 2048u, &vmap, 16 * c,
+                        (int)(row / bs * kD), full + 8 * (st));
+        }
       }
       issued = j0 + ntl;
     }
@@ -339,7 +351,9 @@ __global__ void __launch_bounds__(kThreads)
         mma_commit(bars.k_empty(st));
       }
     } else {
-      const uint32_t idpv = idesc_e4m3(128, 128, 0, 1);
+      // V as loaded: token-major pages give an MN-major B (dims contiguous, 128-byte swizzle);
+      // dimension-major pages a K-major B of 16-token core-matrix blocks, 2 KB apart along K
+      const uint32_t idpv = idesc_e4m3(128, 128, 0, kVdm ? 0 : 1);
       for (int j = 0; ok && j < n_tiles; j++) {
         const int pb = j & 1, st = j % kStages;
         if (!mbar_wait(bars.p_full(pb), (j >> 1) & 1, abort)) { ok = false; break; }
@@ -350,7 +364,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int k = 0; k < 4; k++)
           mma_e4m3(tmem + kColO + pb * 128, sdesc_sw128(pa + 32 * k, 16, 1024),
-                   sdesc_sw128(vt + 4096 * k, 16384, 1024), idpv, (j >= 2 || k > 0) ? 1u : 0u);
+                   kVdm ? sdesc_none(vt + 4096 * k, 2048, 128) : sdesc_sw128(vt + 4096 * k, 16384, 1024), idpv,
+                   (j >= 2 || k > 0) ? 1u : 0u);
         mma_commit(bars.pv_done(pb));
         mma_commit(bars.v_empty(st));
       }
@@ -395,7 +410,7 @@ __global__ void __launch_bounds__(kThreads)
     auto tok_page = [&](int jt, int& pg) -> bool {
       const int t = t0 + jt * kTile + kt;
       const bool rd = jt < n_tiles && t >= sp.lo && t < t1;
-      pg = __ldg(p.block_table + (int64_t)b * p.max_blocks + (rd ? t >> bs_sh : 0));
+      pg = page_at(p, b, rd ? t >> bs_sh : 0);
       return rd;
     };
     auto tok_scales = [&](int jt, bool rd, int pg, float& ks, float& vs) -> bool {
@@ -536,10 +551,16 @@ __global__ void __launch_bounds__(kThreads)
         if (!mbar_wait(bars.v_full(st), (j / kStages) & 1, abort)) set_abort(abort, p.status);
         const uint32_t mw = wq == 0 ? vmk.x : wq == 1 ? vmk.y : wq == 2 ? vmk.z : vmk.w;
         if (!((mw >> lane) & 1)) {
-          const uint32_t vrow = sbase + kOffV + st * kVStageBytes + 128 * kt;
+          if constexpr (!kVdm) {
+            const uint32_t vrow = sbase + kOffV + st * kVStageBytes + 128 * kt;
 #pragma unroll
-          for (int c = 0; c < 8; c++)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + 16 * c), "r"(0));
+            for (int c = 0; c < 8; c++)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + 16 * c), "r"(0));
+          } else {
+            // the token's byte in each of the 128 dimension rows of its 16-token block
+            const uint32_t vcol = sbase + kOffV + st * kVStageBytes + (kt >> 4) * 2048u + (kt & 15);
+            for (int d = 0; d < kD; d++) asm volatile("st.shared.u8 [%0], %1;" ::"r"(vcol + 16 * d), "h"((uint16_t)0));
+          }
         }
         fence_proxy_async();
       }
@@ -813,6 +834,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
+// Dimension-major V: [pages * Hkv * D rows][bs bytes], boxes of 128 rows x 16 bytes, unswizzled.
+bool encode_vdm_map(CUtensorMap* map, const void* base, int64_t rows, int bs) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)bs, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)bs};
+  cuuint32_t box[2] = {16, (cuuint32_t)kD};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t rows, int bs) {
   auto enc = get_encoder();
   if (!enc) return false;
@@ -830,6 +864,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t rows, int bs) 
 bool tc_fp8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   return d.kv_dtype == TLLM_FP8_E4M3 && d.head_dim == kD && rows >= 1 && rows <= 64 &&
+         (d.v_layout == TLLM_V_TOKEN_MAJOR || (d.v_layout == TLLM_V_DIM_MAJOR && bs >= 16)) &&
          (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
 }
@@ -842,16 +877,18 @@ bool tc_fp8_pointers_ok(const Params& p) {
 cudaError_t launch_partial_tc_fp8(const Params& p, cudaStream_t stream) {
   CUtensorMap km, vm;
   const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.bs;
-  if (!encode_cache_map(&km, p.k_cache, rows, p.bs) || !encode_cache_map(&vm, p.v_cache, rows, p.bs))
+  if (!encode_cache_map(&km, p.k_cache, rows, p.bs) ||
+      !(p.v_dim_major ? encode_vdm_map(&vm, p.v_cache, rows / p.bs * kD, p.bs) : encode_cache_map(&vm, p.v_cache, rows, p.bs)))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(partial_tc_fp8_kernel), (int)kSmemBytes);
+  auto kern = p.v_dim_major ? partial_tc_fp8_kernel<true> : partial_tc_fp8_kernel<false>;
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   // persistent grid: one CTA per SM (the shared memory allows one), at most one per item
   const int n_items = p.B * p.Hkv * p.num_splits;
   const int n_sm = sm_count();
   if (n_sm <= 0) return cudaErrorInvalidValue;
   dim3 grid(n_items < n_sm ? n_items : n_sm);
-  partial_tc_fp8_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, km, vm);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(p, km, vm);
   return cudaGetLastError();
 }
 

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads)
       const int tt = t0 + jt * kT, first = bs < kT ? tt + lane * bs : tt;
       const int last = bs < kT ? first + bs : tt + kT;
       if (max(first, sp.lo) >= min(last, t1)) return -1;
-      const int pg = p.block_table[(int64_t)b * p.max_blocks + (first >> bs_sh)];
+      const int pg = page_at(p, b, first >> bs_sh);
       if (pg < 0 || pg >= p.num_pages) {
         atomicOr(p.status, TLLM_FLAG_BAD_PAGE);
         return -1;
@@ -737,6 +737,7 @@ cudaError_t launch_d(const Params& p, cudaStream_t stream) {
 bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   return d.kv_dtype == TLLM_INT8 && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) && (d.head_dim == 128 || d.head_dim == 256) &&
+         d.v_layout == TLLM_V_TOKEN_MAJOR &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
 }

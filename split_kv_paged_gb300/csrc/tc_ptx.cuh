@@ -183,6 +183,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory matrix descriptor, no swizzle (interleaved core matrices of 8 rows x 16 bytes,
+// each stored as 128 contiguous bytes). For a K-major operand, lbo is the byte distance between
+// core matrices adjacent along K and sbo between core matrices adjacent along M / N.
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version of tcgen05; layout type 0 (no swizzle)
+  return d;
+}
+
 // Instruction descriptor of kind::f8f6f4 with e4m3 A and B and an f32 accumulator.
 // a_mn / b_mn: operand is MN-major (1) instead of K-major (0).
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, int a_mn, int b_mn) {

@@ -122,7 +122,6 @@ def _fake_call(name, plan, ws_bytes=None, **over):
 @pytest.mark.parametrize("over,status", [
     (dict(q=None), B.TLLM_ERR_INVALID_ARG),
     (dict(k=None), B.TLLM_ERR_INVALID_ARG),
-    (dict(bt=None), B.TLLM_ERR_INVALID_ARG),
     (dict(ctx=None), B.TLLM_ERR_INVALID_ARG),
     (dict(out=None), B.TLLM_ERR_INVALID_ARG),
     (dict(scales=None), B.TLLM_ERR_INVALID_ARG),        # FP8 KV needs scales
@@ -288,3 +287,26 @@ def test_planner_fits_the_ragged_batch_in_one_item_wave(lib, bs):
     assert counts[0] == plan.num_splits > 92
     sizes = [B.tllm_decode_attn_split_range(plan, wl.ctx[0], wl.Lq, 0, plan.num_splits, s) for s in range(counts[0])]
     assert max(t1 - t0 for t0, t1, _ in sizes) == plan.min_chunk
+
+
+def test_contiguous_cache_needs_every_request_block(lib):
+    """Without a block table the cache must hold batch x max_blocks_per_seq pages; a smaller
+    one is refused before any launch."""
+    wl = W.mtp4_fp8_long(batch=4, ctx=1000)
+    desc = B.desc_for(wl, num_pages=4 * wl.max_blocks - 1)
+    plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=2)
+    ws = B.tllm_workspace(ctypes.pointer(plan), 256, plan.workspace_bytes)
+    st = B.lib().tllm_decode_attn_splitkv(256, 256, 256, None, 256, wl.Lq, 256, None, 0, 2, ctypes.byref(ws), 256,
+                                          None)
+    assert st == B.TLLM_ERR_INVALID_ARG
+
+
+def test_dim_major_v_routes_to_kernels_that_read_it(lib):
+    """AUTO with a transposed V cache: the FP8 tensor-core kernel for FP8 KV with pages of 16 or
+    more tokens; the CUDA-core generic kernel otherwise (16-bit or INT8 KV, 8-token pages)."""
+    def plan(wl):
+        return B.tllm_decode_attn_plan(B.desc_for(wl, v_layout=B.TLLM_V_DIM_MAJOR), wl.B, wl.Lq, 0,
+                                       host_ctx_lens=wl.ctx)
+    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000)).kernel == B.TLLM_KERNEL_TC_FP8
+    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000, bs=8)).kernel == B.TLLM_KERNEL_GENERIC
+    assert plan(W.window_sink_bf16(batch=2)).kernel == B.TLLM_KERNEL_GENERIC

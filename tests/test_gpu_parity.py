@@ -649,3 +649,88 @@ def test_tc_i8_repeatable():
         for _ in range(4):
             again, _, _ = run_gpu(inp, TCI8, splits=S)
             assert torch.equal(first, again), f"S={plan.num_splits}: outputs differ between runs"
+
+
+# --- contiguous cache (no block table) ----------------------------------------------
+
+def _contiguous(inp):
+    """The same problem in a contiguous cache: block i of request b moved to page
+    b * max_blocks + i; unused pages poisoned. Returns the new caches and scales."""
+    wl = inp.wl
+    n_pages = wl.B * wl.max_blocks
+    shape = (n_pages,) + tuple(inp.k_cache.shape[1:])
+    k = torch.empty(shape, dtype=inp.k_cache.dtype, device="cuda")
+    v = torch.empty_like(k)
+    if wl.kv_dtype == "e4m3":
+        k.view(torch.uint8).fill_(0x7F)
+        v.view(torch.uint8).fill_(0x7F)
+    elif wl.kv_dtype == "i8":
+        k.zero_()
+        v.zero_()
+    else:
+        k.fill_(float("nan"))
+        v.fill_(float("nan"))
+    sc = None
+    if inp.kv_scales is not None:
+        sc = torch.full((2, n_pages) + tuple(inp.kv_scales.shape[2:]), float("nan"), dtype=torch.float32,
+                        device="cuda")
+    for b in range(wl.B):
+        n = (int(inp.context_lens[b]) + wl.bs - 1) // wl.bs
+        src = inp.block_table[b, :n].long()
+        dst = torch.arange(b * wl.max_blocks, b * wl.max_blocks + n, device="cuda")
+        k[dst] = inp.k_cache[src]
+        v[dst] = inp.v_cache[src]
+        if sc is not None:
+            sc[:, dst] = inp.kv_scales[:, src]
+    return k, v, sc, n_pages
+
+
+@pytest.mark.parametrize("wl,kernel", [
+    (W.mtp4_fp8_long(batch=3, ctx=1).replace(ctx=[5000, 777, 3]), B.TLLM_KERNEL_TC_FP8),
+    (W.verify16_int8().replace(ctx=[3000, 700]), B.TLLM_KERNEL_TC_I8),
+    (W.window_sink_bf16(batch=3).replace(ctx=[6000, 4097, 17]), B.TLLM_KERNEL_TC_B16),
+    (W.single_decode().replace(ctx=[2048, 300]), B.TLLM_KERNEL_SIMT),
+    (W.single_decode().replace(ctx=[2048, 300]), B.TLLM_KERNEL_GENERIC),
+])
+def test_contiguous_cache_without_block_table(wl, kernel):
+    """block_table = NULL: request b's block i is page b * max_blocks + i. The result equals
+    the oracle on the paged layout of the same data."""
+    inp = _inputs(wl, 190, poison=False)
+    ref, _ = oracle_out(inp)
+    k, v, sc, n_pages = _contiguous(inp)
+    for S in (1, 3):
+        plan = plan_for(wl, kernel, S, num_pages=n_pages)
+        assert plan.kernel == kernel
+        ws = poisoned_workspace(plan)
+        out = new_out(wl)
+        B.tllm_decode_attn_splitkv(inp.q, k, v, None, inp.context_lens, wl.Lq, sc, inp.sinks, wl.window, S, ws,
+                                   out)
+        torch.cuda.synchronize()
+        assert not (B.tllm_decode_attn_read_status(ws) & (B.TLLM_FLAG_TIMEOUT | B.TLLM_FLAG_BAD_PAGE))
+        assert_close(out, ref, wl.kv_dtype, f"contiguous {wl.name} kernel {kernel} S{S}")
+
+
+# --- dimension-major ("transposed") V cache ----------------------------------------------
+
+@pytest.mark.parametrize("bs", [16, 32, 128])
+@pytest.mark.parametrize("kernel", [B.TLLM_KERNEL_TC_FP8, B.TLLM_KERNEL_GENERIC])
+def test_dim_major_v_cache(bs, kernel):
+    """V stored [num_pages, Hkv, D, bs] (aiter PR #5628, Performance table: the transposed V
+    layout): the same problem as the token-major cache, checked against the oracle on the
+    token-major data. Partial tiles (window, short requests) zero the unread tokens' columns."""
+    wl = W.mtp4_fp8_long(batch=4, ctx=1).replace(ctx=[7000, 1500, 130, 5], bs=bs, window=700, sinks=True,
+                                                 extra_pages=3)
+    inp = _inputs(wl, 200 + bs)
+    ref, _ = oracle_out(inp)
+    v_dm = inp.v_cache.transpose(-1, -2).contiguous()
+    for S in (1, 3):
+        desc = B.desc_for(wl, kernel, num_pages=inp.num_pages, v_layout=B.TLLM_V_DIM_MAJOR)
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        assert plan.kernel == kernel
+        ws = poisoned_workspace(plan)
+        out = new_out(wl)
+        B.tllm_decode_attn_splitkv(inp.q, inp.k_cache, v_dm, inp.block_table, inp.context_lens, wl.Lq,
+                                   inp.kv_scales, inp.sinks, wl.window, S, ws, out)
+        torch.cuda.synchronize()
+        assert not (B.tllm_decode_attn_read_status(ws) & B.TLLM_FLAG_TIMEOUT)
+        assert_close(out, ref, wl.kv_dtype, f"dim-major V bs{bs} kernel {kernel} S{S}")
