@@ -93,6 +93,17 @@ typedef enum {
                                         (the transposed V cache) */
 } tllm_v_layout;
 
+/* Element type of the normalised partial outputs (split records) in the workspace. fp32 by
+ * default; a 16-bit record halves the record traffic and the workspace (aiter PR #5628,
+ * Changes: a 16-bit partial output per row plus fp32 scalars) at the cost of one rounding of
+ * each partial output: 2^-9 relative for bf16, 2^-11 for f16 (whose range ends at 65504, so
+ * f16 records suit caches whose dequantised values stay below that). The log-sum-exp stays fp32. */
+typedef enum {
+  TLLM_RECORD_F32 = 0,
+  TLLM_RECORD_BF16 = 1,
+  TLLM_RECORD_F16 = 2
+} tllm_record_type;
+
 /* Device status bits written into the workspace header. */
 #define TLLM_FLAG_CTX_CLAMPED   0x1u  /* some context_lens[b] was < 0 or > max_blocks*bs; clamped */
 #define TLLM_FLAG_BAD_PAGE      0x2u  /* some referenced page id was outside [0, num_pages); masked */
@@ -110,6 +121,7 @@ typedef struct {
   float softmax_scale;               /* 0 => 1/sqrt(head_dim) */
   tllm_kernel kernel;                /* TLLM_KERNEL_AUTO unless a test pins a variant */
   tllm_v_layout v_layout;            /* TLLM_V_TOKEN_MAJOR unless the V cache is transposed */
+  tllm_record_type record_type;      /* TLLM_RECORD_F32 unless 16-bit split records are wanted */
 } tllm_decode_attn_desc;
 
 /* Host POD produced by tllm_decode_attn_plan; copy it freely. */
@@ -214,7 +226,8 @@ tllm_status tllm_decode_attn_combine(const void* q, const void* k_cache, const v
  *   status  uint32 status word (TLLM_FLAG_*)
  *   lse     fp32 [batch*Hkv][max_splits][rows], LSE of the split in log2 units
  *           (log2 sum_t 2^(s_t * log2 e)); -inf for a split with no visible key
- *   o       fp32 [batch*Hkv][max_splits][rows][head_dim], normalised partial output
+ *   o       [batch*Hkv][max_splits][rows][head_dim], normalised partial output in the
+ *           desc's record_type (fp32, bf16 or f16)
  * Row r of (request b, kv head g) is query row r / G of query head g*G + r % G.
  */
 tllm_status tllm_decode_attn_workspace_layout(const tllm_decode_attn_plan_t* plan, size_t* status_off,

@@ -31,6 +31,8 @@ tllm_status check_desc(const tllm_decode_attn_desc* d) {
   if (d->block_size > 256) return TLLM_ERR_UNSUPPORTED;
   if (d->kernel < TLLM_KERNEL_AUTO || d->kernel > TLLM_KERNEL_TC_B16) return TLLM_ERR_INVALID_ARG;
   if (d->v_layout != TLLM_V_TOKEN_MAJOR && d->v_layout != TLLM_V_DIM_MAJOR) return TLLM_ERR_INVALID_ARG;
+  if (d->record_type != TLLM_RECORD_F32 && d->record_type != TLLM_RECORD_BF16 && d->record_type != TLLM_RECORD_F16)
+    return TLLM_ERR_INVALID_ARG;
   return TLLM_OK;
 }
 
@@ -283,8 +285,9 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
   out_plan->kernel = kernel;
   out_plan->rows = rows;
   const size_t units = (size_t)batch * d.num_kv_heads * S * rows;
+  const size_t rec_bytes = d.record_type == TLLM_RECORD_F32 ? 4 : 2;
   out_plan->workspace_bytes = kHeaderBytes + align256(units * sizeof(float)) +
-                              align256(units * (size_t)d.head_dim * sizeof(float));
+                              align256(units * (size_t)d.head_dim * rec_bytes);
   return TLLM_OK;
 }
 
@@ -378,6 +381,7 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->kv_dtype = d.kv_dtype;
   p->out_dtype = d.out_dtype;
   p->v_dim_major = d.v_layout == TLLM_V_DIM_MAJOR;
+  p->rec_type = d.record_type;
   // alignment the chosen kernel's copies need (TMA boxes, 16-byte loads and stores)
   bool aligned = true;
   switch (pl.kernel) {

@@ -25,26 +25,47 @@ namespace {
 
 constexpr int kWarps = 8;
 
-// V consecutive floats of a record row
-template <int V>
+// V consecutive elements of a record row (fp32, bf16 or f16), widened to fp32
+template <int V, typename RT>
 struct VecF {
   float v[V];
-  __device__ __forceinline__ void load(const float* x) {
+  __device__ __forceinline__ void load(const RT* x) {
+    if constexpr (sizeof(RT) == 4) {
 #pragma unroll
-    for (int c = 0; c < V; c += 4 > V ? V : 4) {
-      if constexpr (V >= 4) {
-        const float4 a = *reinterpret_cast<const float4*>(x + c);
-        v[c] = a.x; v[c + 1] = a.y; v[c + 2] = a.z; v[c + 3] = a.w;
-      } else if constexpr (V == 2) {
-        const float2 a = *reinterpret_cast<const float2*>(x);
-        v[0] = a.x; v[1] = a.y;
+      for (int c = 0; c < V; c += (V < 4 ? V : 4)) {
+        if constexpr (V >= 4) {
+          const float4 a = *reinterpret_cast<const float4*>(x + c);
+          v[c] = a.x; v[c + 1] = a.y; v[c + 2] = a.z; v[c + 3] = a.w;
+        } else {
+          const float2 a = *reinterpret_cast<const float2*>(x);
+          v[0] = a.x; v[1] = a.y;
+        }
+      }
+    } else {
+      // V 16-bit values: 4 bytes (V = 2), 8 (V = 4) or 16 (V = 8) in one load
+      uint32_t w[V / 2];
+      if constexpr (V == 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(x);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      } else if constexpr (V == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(x);
+        w[0] = a.x; w[1] = a.y;
       } else {
-        v[0] = *x;
+        w[0] = *reinterpret_cast<const uint32_t*>(x);
+      }
+#pragma unroll
+      for (int c = 0; c < V / 2; c++) {
+        float2 f;
+        if constexpr (std::is_same<RT, __nv_bfloat16>::value)
+          f = make_float2(__uint_as_float(w[c] << 16), __uint_as_float(w[c] & 0xffff0000u));
+        else
+          f = __half22float2(*reinterpret_cast<const __half2*>(&w[c]));
+        v[2 * c] = f.x;
+        v[2 * c + 1] = f.y;
       }
     }
   }
 };
-
 
 // V output elements from fp32 values: one 8- or 16-byte store for 16-bit outputs
 template <typename OT, int V>
@@ -80,8 +101,8 @@ __device__ __forceinline__ void store_row(OT* out, const float* a, float mul) {
   }
 }
 
-// D columns, WPR warps per row, kG splits per load group
-template <typename OT, int D, int WPR, int kG>
+// D columns, WPR warps per row, kG splits per load group, RT the record element type
+template <typename OT, int D, int WPR, int kG, typename RT>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Params p) {
   constexpr int V = D / 32;                      // columns per lane
   constexpr int RPC = kWarps / WPR;              // rows per CTA
@@ -101,7 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Params p) {
   pdl_wait();                                    // the partial grid's records are complete
   const int rr = live ? r : 0;
   const float* lse = p.ws_lse + (int64_t)u * p.max_splits * p.R + rr;
-  const float* o = p.ws_o + ((int64_t)u * p.max_splits * p.R + rr) * D + col;
+  const RT* o = reinterpret_cast<const RT*>(p.ws_o) + ((int64_t)u * p.max_splits * p.R + rr) * D + col;
   const int64_t stride = (int64_t)p.R * D;
 
   // this warp's splits: wsub, wsub + WPR, ...; lane k of a group holds the LSE of its k-th split
@@ -112,7 +133,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(Params p) {
   for (int k0 = 0; k0 < mine; k0 += kG) {
     const int sl = wsub + (k0 + lane) * WPR;
     const float ls = lane < kG && k0 + lane < mine ? lse[(int64_t)sl * p.R] : -INFINITY;
-    VecF<V> x[kG];
+    VecF<V, RT> x[kG];
 #pragma unroll
     for (int k = 0; k < kG; k++)
       if (k0 + k < mine) x[k].load(o + (int64_t)(wsub + (k0 + k) * WPR) * stride);
@@ -211,7 +232,11 @@ template <typename OT, int D, int WPR>
 cudaError_t launch_wpr(const Params& p, cudaStream_t stream) {
   constexpr int kG = D >= 256 ? 4 : 8;
   const dim3 grid(p.B * p.Hkv, (p.R + kWarps / WPR - 1) / (kWarps / WPR));
-  return launch_pdl(combine_kernel<OT, D, WPR, kG>, grid, stream, p);
+  switch (p.rec_type) {
+    case TLLM_RECORD_BF16: return launch_pdl(combine_kernel<OT, D, WPR, kG, __nv_bfloat16>, grid, stream, p);
+    case TLLM_RECORD_F16: return launch_pdl(combine_kernel<OT, D, WPR, kG, __half>, grid, stream, p);
+    default: return launch_pdl(combine_kernel<OT, D, WPR, kG, float>, grid, stream, p);
+  }
 }
 
 template <typename OT, int D>

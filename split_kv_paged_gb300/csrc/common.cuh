@@ -30,14 +30,36 @@ struct Params {
   void* out;
   uint32_t* status;                 // workspace status word
   float* ws_lse;                    // [B*Hkv][max_splits][R]
-  float* ws_o;                      // [B*Hkv][max_splits][R][D]
+  float* ws_o;                      // [B*Hkv][max_splits][R][D] in rec_type (fp32, or 16-bit viewed through it)
   int B, Lq, Hq, Hkv, G, D, R, bs;
   int max_blocks, num_pages, window, num_splits, max_splits, min_chunk, align;
   int max_ctx;                      // max_blocks * bs: lengths are clamped to it
   float scale_log2;                 // softmax scale * log2(e)
   int q_dtype, kv_dtype, out_dtype;
   int v_dim_major;                  // v_cache [num_pages, Hkv, D, bs] (TLLM_V_DIM_MAJOR)
+  int rec_type;                     // tllm_record_type of the split records
 };
+
+// Element i of the split-record area: fp32, or bf16 / f16 when the plan asked for 16-bit records.
+__device__ __forceinline__ void store_rec(const Params& p, int64_t i, float v) {
+  if (p.rec_type == TLLM_RECORD_F32) p.ws_o[i] = v;
+  else if (p.rec_type == TLLM_RECORD_BF16) reinterpret_cast<__nv_bfloat16*>(p.ws_o)[i] = __float2bfloat16_rn(v);
+  else reinterpret_cast<__half*>(p.ws_o)[i] = __float2half_rn(v);
+}
+// Four consecutive record elements from i (i a multiple of 4): one 16- or 8-byte store.
+__device__ __forceinline__ void store_rec4(const Params& p, int64_t i, float4 v) {
+  if (p.rec_type == TLLM_RECORD_F32) {
+    *reinterpret_cast<float4*>(p.ws_o + i) = v;
+  } else if (p.rec_type == TLLM_RECORD_BF16) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.ws_o) + i) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  } else {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(p.ws_o) + i) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
 
 // ---- the split rule (host and device) -------------------------------------------
 // tiny-llm PR #11, design section: each partial CTA derives its own logical range

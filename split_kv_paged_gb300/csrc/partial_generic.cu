@@ -186,10 +186,10 @@ __global__ void __launch_bounds__(kThreads) partial_generic_kernel(Params p) {
       }
     } else {
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* o = p.ws_o + ((int64_t)u_split * p.R + r) * D;
+      const int64_t o = ((int64_t)u_split * p.R + r) * D;
       for (int c = 0; c < DC; c++) {
         const int d = tid + c * kThreads;
-        if (d < D) o[d] = acc[j][c] * inv;
+        if (d < D) store_rec(p, o + d, acc[j][c] * inv);
       }
       if (tid == 0) p.ws_lse[(int64_t)u_split * p.R + r] = l > 0.f ? m + log2f(l) : -INFINITY;
     }

@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
       if (p.sinks && M != -INFINITY) den += ex2s(p.sinks[h] * kLog2e - M);
       store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + qi) * p.Hq + h) * D + d, L > 0.f ? O / den : 0.f);
     } else {
-      p.ws_o[((int64_t)u_split * p.R + r) * D + d] = L > 0.f ? O / L : 0.f;
+      store_rec(p, ((int64_t)u_split * p.R + r) * D + d, L > 0.f ? O / L : 0.f);
       if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
   }

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads)
         const int i = r / p.G, hq = g * p.G + r % p.G;
         store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + i) * p.Hq + hq) * kD + d, 0.f);
       } else {
-        p.ws_o[((int64_t)u_split * p.R + r) * kD + d] = 0.f;
+        store_rec(p, ((int64_t)u_split * p.R + r) * kD + d, 0.f);
         if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = -INFINITY;
       }
     }
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kThreads)
             if (den > 0.f) mul = 1.f / (p.sinks ? den + ex2(p.sinks[qh] * kLog2e - M[r]) : den);
             store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + qi) * p.Hq + qh) * kD + L, val * mul);
           } else {
-            p.ws_o[((int64_t)u_split * p.R + r) * kD + L] = den > 0.f ? val / den : 0.f;
+            store_rec(p, ((int64_t)u_split * p.R + r) * kD + L, den > 0.f ? val / den : 0.f);
             if (L == 0) p.ws_lse[(int64_t)u_split * p.R + r] = den > 0.f ? M[r] + log2f(den) : -INFINITY;
           }
         }

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads)
         const int i = r / p.G, hq = g * p.G + r % p.G;
         store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + i) * p.Hq + hq) * kD + d, 0.f);
       } else {
-        p.ws_o[((int64_t)u_split * p.R + r) * kD + d] = 0.f;
+        store_rec(p, ((int64_t)u_split * p.R + r) * kD + d, 0.f);
         if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = -INFINITY;
       }
     }
@@ -778,8 +778,12 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t ob = ((int64_t)(b * p.Lq + qi) * p.Hq + qh) * kD + c_keep;
         // this thread's 32 columns of row r as 16-byte stores: fp32 (split record or fp32
         // output) four values per store, a 16-bit output eight
-        float* dst32 = finalize ? static_cast<float*>(p.out) + ob : p.ws_o + ((int64_t)u_split * p.R + r) * kD + c_keep;
-        const bool out16 = finalize && p.out_dtype != TLLM_F32, bf = p.out_dtype == TLLM_BF16;
+        // (a 16-bit split record takes the 16-bit path too, into the record area)
+        const int64_t rec = ((int64_t)u_split * p.R + r) * kD + c_keep;
+        float* dst32 = finalize ? static_cast<float*>(p.out) + ob : p.ws_o + rec;
+        uint16_t* dst16 = finalize ? static_cast<uint16_t*>(p.out) + ob : reinterpret_cast<uint16_t*>(p.ws_o) + rec;
+        const bool out16 = finalize ? p.out_dtype != TLLM_F32 : p.rec_type != TLLM_RECORD_F32;
+        const bool bf = finalize ? p.out_dtype == TLLM_BF16 : p.rec_type == TLLM_RECORD_BF16;
         uint32_t pk[4];
 #pragma unroll
         for (int i4 = 0; i4 < 8; i4++) {
@@ -802,8 +806,7 @@ __global__ void __launch_bounds__(kThreads)
               pk[2 * (i4 & 1) + 1] = *reinterpret_cast<const uint32_t*>(&h1);
             }
             if (i4 & 1)
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + ob + 4 * (i4 - 1)) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(dst16 + 4 * (i4 - 1)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
       }

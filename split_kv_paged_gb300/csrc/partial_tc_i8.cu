@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads)
         const int i = r / p.G, hq = g * p.G + r % p.G;
         store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + i) * p.Hq + hq) * D + d, 0.f);
       } else {
-        p.ws_o[((int64_t)u_split * p.R + r) * D + d] = 0.f;
+        store_rec(p, ((int64_t)u_split * p.R + r) * D + d, 0.f);
         if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = -INFINITY;
       }
     }
@@ -634,8 +634,8 @@ __global__ void __launch_bounds__(kThreads)
           for (int k = 0; k < 8; k++) {
             const int rr = 4 * k + (lane >> 3), rg = 32 * (warp & 3) + rr;
             if (rg < p.R)
-              *reinterpret_cast<float4*>(p.ws_o + ((int64_t)u_split * p.R + rg) * D + c0 + 4 * (lane & 7)) =
-                  *reinterpret_cast<const float4*>(stage + rr * kEpiStride + 4 * (lane & 7));
+              store_rec4(p, ((int64_t)u_split * p.R + rg) * D + c0 + 4 * (lane & 7),
+                         *reinterpret_cast<const float4*>(stage + rr * kEpiStride + 4 * (lane & 7)));
           }
         } else if (p.out_dtype == TLLM_F32) {
           // lane: row 4k + lane / 8 of the warp's 32, columns c0 + 4 (lane % 8) .. + 3

@@ -310,3 +310,18 @@ def test_dim_major_v_routes_to_kernels_that_read_it(lib):
     assert plan(W.mtp4_fp8_long(batch=2, ctx=4000)).kernel == B.TLLM_KERNEL_TC_FP8
     assert plan(W.mtp4_fp8_long(batch=2, ctx=4000, bs=8)).kernel == B.TLLM_KERNEL_GENERIC
     assert plan(W.window_sink_bf16(batch=2)).kernel == B.TLLM_KERNEL_GENERIC
+
+
+def test_sixteen_bit_records_halve_the_record_area(lib):
+    """A 16-bit record plan needs half the partial-output bytes of an fp32 one; the LSE area is
+    unchanged."""
+    wl = W.ragged_fp8(bs=128)
+    plans = [B.tllm_decode_attn_plan(B.desc_for(wl, record_type=r), wl.B, wl.Lq, 0, host_ctx_lens=wl.ctx)
+             for r in (B.TLLM_RECORD_F32, B.TLLM_RECORD_BF16, B.TLLM_RECORD_F16)]
+    f32, bf16, f16 = plans
+    assert bf16.num_splits == f32.num_splits and bf16.workspace_bytes == f16.workspace_bytes
+    _, lo, oo = B.tllm_decode_attn_workspace_layout(f32)
+    o32 = f32.workspace_bytes - oo
+    _, lo16, oo16 = B.tllm_decode_attn_workspace_layout(bf16)
+    assert (lo16, oo16) == (lo, oo)
+    assert abs((bf16.workspace_bytes - oo16) * 2 - o32) <= 512

@@ -212,14 +212,19 @@ def test_stage_entry_points_compose(kernel):
     assert torch.equal(out, ref_out)
 
 
+REC_TORCH = {B.TLLM_RECORD_F32: torch.float32, B.TLLM_RECORD_BF16: torch.bfloat16, B.TLLM_RECORD_F16: torch.float16}
+
+
+@pytest.mark.parametrize("rec", [B.TLLM_RECORD_F32, B.TLLM_RECORD_BF16, B.TLLM_RECORD_F16])
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_partial_records_match_oracle_partials(kernel):
+def test_partial_records_match_oracle_partials(kernel, rec):
     """The split records themselves: O_s and LSE_s of every split equal the oracle's
-    attention restricted to that split's key range."""
+    attention restricted to that split's key range, in each record type."""
     wl = W.mtp4_fp8_long(batch=2, ctx=1).replace(ctx=[3001, 1500], window=700, sinks=True)
     inp = _inputs(wl, 12)
     S = 3
-    plan = plan_for(wl, kernel, S, num_pages=inp.num_pages)
+    desc = B.desc_for(wl, kernel, num_pages=inp.num_pages, record_type=rec)
+    plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
     ws = poisoned_workspace(plan)
     out = new_out(wl)
     B.tllm_decode_attn_partial(inp.q, inp.k_cache, inp.v_cache, inp.block_table, inp.context_lens, wl.Lq,
@@ -228,8 +233,9 @@ def test_partial_records_match_oracle_partials(kernel):
     so, lo, oo = B.tllm_decode_attn_workspace_layout(plan)
     R, D, Smax = plan.rows, wl.D, plan.max_splits
     lse = ws.buffer[lo:lo + wl.B * wl.Hkv * Smax * R * 4].view(torch.float32).view(wl.B, wl.Hkv, Smax, R).cpu()
-    orec = ws.buffer[oo:oo + wl.B * wl.Hkv * Smax * R * D * 4].view(torch.float32).view(
-        wl.B, wl.Hkv, Smax, R, D).cpu()
+    esz = torch.finfo(REC_TORCH[rec]).bits // 8
+    orec = ws.buffer[oo:oo + wl.B * wl.Hkv * Smax * R * D * esz].view(REC_TORCH[rec]).view(
+        wl.B, wl.Hkv, Smax, R, D).float().cpu()
     G = wl.G
     for b, ctx in enumerate(wl.ctx):
         t0, t1, n = B.tllm_decode_attn_split_range(plan, ctx, wl.Lq, wl.window, S, 0)
@@ -734,3 +740,27 @@ def test_dim_major_v_cache(bs, kernel):
         torch.cuda.synchronize()
         assert not (B.tllm_decode_attn_read_status(ws) & B.TLLM_FLAG_TIMEOUT)
         assert_close(out, ref, wl.kv_dtype, f"dim-major V bs{bs} kernel {kernel} S{S}")
+
+
+
+# --- 16-bit split records -------------------------------------------------------------
+
+@pytest.mark.parametrize("rec", [B.TLLM_RECORD_BF16, B.TLLM_RECORD_F16])
+@pytest.mark.parametrize("wl,seed", [
+    (W.mtp4_fp8_long(batch=6, ctx=1).replace(ctx=[20000, 12345, 777, 4, 3, 40001], extra_pages=10), 1003),
+    (W.verify16_int8().replace(extra_pages=16), 1002),
+    (W.ragged_fp8(bs=128).replace(extra_pages=4), 1004),
+    (W.window_sink_bf16(batch=5).replace(ctx=[9000, 4097, 300, 2, 1]), 1005),
+    (W.single_decode().replace(extra_pages=8), 1001),
+])
+def test_sixteen_bit_records(wl, seed, rec):
+    """The whole call with bf16 or f16 split records (aiter PR #5628, Changes: a 16-bit partial
+    output per row): the records' one extra rounding stays inside the parity tolerance, at the
+    planner's split count and at a forced larger one."""
+    inp = _inputs(wl, seed)
+    ref, _ = oracle_out(inp)
+    for S in (0, 5):
+        desc = B.desc_for(wl, num_pages=inp.num_pages, record_type=rec)
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        out, _, _ = run_gpu(inp, plan=plan)
+        assert_close(out, ref, wl.kv_dtype, f"{wl.name} records {rec} S={plan.num_splits}")
