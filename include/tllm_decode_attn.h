@@ -104,6 +104,19 @@ typedef enum {
   TLLM_RECORD_F16 = 2
 } tllm_record_type;
 
+/* How the split records are merged. TLLM_COMBINE_KERNEL: a combine kernel launched as a
+ * programmatic dependent of the partial kernel, so its launch overlaps the partial's tail.
+ * TLLM_COMBINE_FUSED: the partial CTA that writes a request's last record merges them all and
+ * no combine kernel runs (tiny-llm PR #11, open question 1: the last CTA merges, an atomic
+ * arrival ticket, no waiting); taken by the CUDA-core few-row kernel when a request's records
+ * are at most 128 KB, else the plan keeps the combine kernel. On a GB300 the fused merge (a
+ * GPU-wide fence, the ticket, then the records read by one CTA) measured about 2 us slower per
+ * call than the overlapped kernel on the single-decode workload, hence the default. */
+typedef enum {
+  TLLM_COMBINE_KERNEL = 0,
+  TLLM_COMBINE_FUSED = 1
+} tllm_combine_mode;
+
 /* Device status bits written into the workspace header. */
 #define TLLM_FLAG_CTX_CLAMPED   0x1u  /* some context_lens[b] was < 0 or > max_blocks*bs; clamped */
 #define TLLM_FLAG_BAD_PAGE      0x2u  /* some referenced page id was outside [0, num_pages); masked */
@@ -122,6 +135,7 @@ typedef struct {
   tllm_kernel kernel;                /* TLLM_KERNEL_AUTO unless a test pins a variant */
   tllm_v_layout v_layout;            /* TLLM_V_TOKEN_MAJOR unless the V cache is transposed */
   tllm_record_type record_type;      /* TLLM_RECORD_F32 unless 16-bit split records are wanted */
+  tllm_combine_mode combine_mode;    /* TLLM_COMBINE_KERNEL unless the fused merge is wanted */
 } tllm_decode_attn_desc;
 
 /* Host POD produced by tllm_decode_attn_plan; copy it freely. */
@@ -136,7 +150,9 @@ typedef struct {
   int32_t split_align;               /* split boundaries sit on multiples of this many tokens */
   int32_t kernel;                    /* tllm_kernel chosen */
   int32_t rows;                      /* packed rows per (request, kv head) = (Hq/Hkv) * query_len */
-  int32_t reserved[7];
+  int32_t fused_combine;             /* 1: the partial kernel merges each request's splits itself
+                                        and no combine kernel is launched (desc.combine_mode) */
+  int32_t reserved[6];
   size_t workspace_bytes;            /* bytes the caller must provide */
 } tllm_decode_attn_plan_t;
 
@@ -223,7 +239,12 @@ tllm_status tllm_decode_attn_combine(const void* q, const void* k_cache, const v
 /*
  * Workspace layout of a plan (byte offsets from workspace->ptr), for callers that
  * inspect the split records:
- *   status  uint32 status word (TLLM_FLAG_*)
+ *   status  uint32 status word (TLLM_FLAG_*), at offset 0
+ *           then, from byte 256 to lse, one uint32 arrival counter per (request, kv head) for
+ *           the fused combine. The status word and the counters (the workspace header) must be
+ *           zero before the first call; every call that completes leaves the counters at zero
+ *           again. After a TLLM_FLAG_TIMEOUT they may not be: tllm_decode_attn_read_status with
+ *           reset clears them.
  *   lse     fp32 [batch*Hkv][max_splits][rows], LSE of the split in log2 units
  *           (log2 sum_t 2^(s_t * log2 e)); -inf for a split with no visible key
  *   o       [batch*Hkv][max_splits][rows][head_dim], normalised partial output in the
@@ -243,7 +264,8 @@ tllm_status tllm_decode_attn_split_range(const tllm_decode_attn_plan_t* plan, in
                                          int32_t* t1, int32_t* nsplits);
 
 /*
- * Read (and optionally clear) the workspace status word. Synchronises `stream`;
+ * Read (and optionally clear) the workspace status word; `reset` also zeroes the arrival
+ * counters of the fused combine when workspace->plan is given. Synchronises `stream`;
  * do not call during graph capture.
  */
 tllm_status tllm_decode_attn_read_status(const tllm_workspace* workspace, uint32_t* flags, int32_t reset,

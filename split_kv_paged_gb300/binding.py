@@ -26,6 +26,8 @@ TLLM_KERNEL_AUTO, TLLM_KERNEL_GENERIC, TLLM_KERNEL_SIMT, TLLM_KERNEL_TC_FP8, TLL
 TLLM_V_TOKEN_MAJOR, TLLM_V_DIM_MAJOR = range(2)
 # tllm_record_type
 TLLM_RECORD_F32, TLLM_RECORD_BF16, TLLM_RECORD_F16 = range(3)
+# tllm_combine_mode
+TLLM_COMBINE_KERNEL, TLLM_COMBINE_FUSED = range(2)
 TLLM_FLAG_CTX_CLAMPED = 0x1
 TLLM_FLAG_BAD_PAGE = 0x2
 TLLM_FLAG_TIMEOUT = 0x4
@@ -47,14 +49,15 @@ class tllm_decode_attn_desc(ctypes.Structure):
                 ("max_blocks_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("softmax_scale", ctypes.c_float), ("kernel", ctypes.c_int), ("v_layout", ctypes.c_int),
-                ("record_type", ctypes.c_int)]
+                ("record_type", ctypes.c_int), ("combine_mode", ctypes.c_int)]
 
 
 class tllm_decode_attn_plan_t(ctypes.Structure):
     _fields_ = [("desc", tllm_decode_attn_desc), ("batch", ctypes.c_int32), ("query_len", ctypes.c_int32),
                 ("window", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("min_chunk", ctypes.c_int32), ("split_align", ctypes.c_int32), ("kernel", ctypes.c_int32),
-                ("rows", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7), ("workspace_bytes", ctypes.c_size_t)]
+                ("rows", ctypes.c_int32), ("fused_combine", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class tllm_workspace(ctypes.Structure):
@@ -120,7 +123,8 @@ def _check(status: int, where: str) -> None:
 
 def make_desc(num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_pages, q_dtype, kv_dtype,
               out_dtype, softmax_scale=0.0, kernel=TLLM_KERNEL_AUTO,
-              v_layout=TLLM_V_TOKEN_MAJOR, record_type=TLLM_RECORD_F32) -> tllm_decode_attn_desc:
+              v_layout=TLLM_V_TOKEN_MAJOR, record_type=TLLM_RECORD_F32,
+              combine_mode=TLLM_COMBINE_KERNEL) -> tllm_decode_attn_desc:
     def code(x):
         if isinstance(x, str):
             return DTYPE_OF_NAME[x]
@@ -130,7 +134,7 @@ def make_desc(num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_se
     return tllm_decode_attn_desc(int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
                                  int(max_blocks_per_seq), int(num_pages), code(q_dtype), code(kv_dtype),
                                  code(out_dtype), float(softmax_scale), int(kernel), int(v_layout),
-                                 int(record_type))
+                                 int(record_type), int(combine_mode))
 
 
 def tllm_decode_attn_plan(desc: tllm_decode_attn_desc, batch: int, query_len: int, window: int = 0,
@@ -250,10 +254,11 @@ def tllm_decode_attn_read_status(workspace: Workspace, reset: bool = False, stre
 # --- convenience over the paged-cache inputs drawn by ``workloads`` -------------------
 
 def desc_for(wl, kernel=TLLM_KERNEL_AUTO, num_pages: Optional[int] = None,
-             v_layout=TLLM_V_TOKEN_MAJOR, record_type=TLLM_RECORD_F32) -> tllm_decode_attn_desc:
+             v_layout=TLLM_V_TOKEN_MAJOR, record_type=TLLM_RECORD_F32,
+             combine_mode=TLLM_COMBINE_KERNEL) -> tllm_decode_attn_desc:
     return make_desc(wl.Hq, wl.Hkv, wl.D, wl.bs, wl.max_blocks, num_pages if num_pages is not None else
                      wl.pages_needed() + wl.extra_pages, wl.q_dtype, wl.kv_dtype, wl.out_dtype, wl.scale, kernel,
-                     v_layout, record_type)
+                     v_layout, record_type, combine_mode)
 
 
 def run(inp, workspace: Workspace, out: torch.Tensor, num_splits: Optional[int] = None, stream=None,

@@ -13,9 +13,12 @@ using namespace tllm;
 
 namespace {
 
-constexpr size_t kHeaderBytes = 256;
+constexpr size_t kHeaderBytes = 256;        // status word; the arrival counters follow
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Status word plus one arrival counter per (request, kv head) for the fused combine.
+size_t header_bytes(int32_t batch, int32_t hkv) { return kHeaderBytes + align256((size_t)batch * hkv * 4); }
 
 bool q_ok(int t) { return t == TLLM_F16 || t == TLLM_BF16 || t == TLLM_F32; }
 bool kv_ok(int t) { return t == TLLM_F16 || t == TLLM_BF16 || t == TLLM_FP8_E4M3 || t == TLLM_INT8; }
@@ -33,6 +36,7 @@ tllm_status check_desc(const tllm_decode_attn_desc* d) {
   if (d->v_layout != TLLM_V_TOKEN_MAJOR && d->v_layout != TLLM_V_DIM_MAJOR) return TLLM_ERR_INVALID_ARG;
   if (d->record_type != TLLM_RECORD_F32 && d->record_type != TLLM_RECORD_BF16 && d->record_type != TLLM_RECORD_F16)
     return TLLM_ERR_INVALID_ARG;
+  if (d->combine_mode != TLLM_COMBINE_KERNEL && d->combine_mode != TLLM_COMBINE_FUSED) return TLLM_ERR_INVALID_ARG;
   return TLLM_OK;
 }
 
@@ -286,8 +290,13 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
   out_plan->rows = rows;
   const size_t units = (size_t)batch * d.num_kv_heads * S * rows;
   const size_t rec_bytes = d.record_type == TLLM_RECORD_F32 ? 4 : 2;
-  out_plan->workspace_bytes = kHeaderBytes + align256(units * sizeof(float)) +
+  out_plan->workspace_bytes = header_bytes(batch, d.num_kv_heads) + align256(units * sizeof(float)) +
                               align256(units * (size_t)d.head_dim * rec_bytes);
+  // Fused combine, when asked for: the CTA that writes a request's last split record merges
+  // them all, so no combine kernel is launched. Only where that merge is small next to the
+  // call: the CUDA-core few-row kernel with at most 128 KB of records per request.
+  out_plan->fused_combine = d.combine_mode == TLLM_COMBINE_FUSED && kernel == TLLM_KERNEL_SIMT && S > 1 &&
+                            (size_t)S * rows * d.head_dim * rec_bytes <= ((size_t)128 << 10);
   return TLLM_OK;
 }
 
@@ -296,8 +305,9 @@ tllm_status tllm_decode_attn_workspace_layout(const tllm_decode_attn_plan_t* pla
   if (!plan) return TLLM_ERR_INVALID_ARG;
   const size_t units = (size_t)plan->batch * plan->desc.num_kv_heads * plan->max_splits * plan->rows;
   if (status_off) *status_off = 0;
-  if (lse_off) *lse_off = kHeaderBytes;
-  if (o_off) *o_off = kHeaderBytes + align256(units * sizeof(float));
+  const size_t hb = header_bytes(plan->batch, plan->desc.num_kv_heads);
+  if (lse_off) *lse_off = hb;
+  if (o_off) *o_off = hb + align256(units * sizeof(float));
   return TLLM_OK;
 }
 
@@ -357,6 +367,7 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->out = out;
   char* base = static_cast<char*>(ws->ptr);
   p->status = reinterpret_cast<uint32_t*>(base + so);
+  p->counters = reinterpret_cast<uint32_t*>(base + kHeaderBytes);
   p->ws_lse = reinterpret_cast<float*>(base + lo);
   p->ws_o = reinterpret_cast<float*>(base + oo);
   p->B = pl.batch;
@@ -382,6 +393,7 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->out_dtype = d.out_dtype;
   p->v_dim_major = d.v_layout == TLLM_V_DIM_MAJOR;
   p->rec_type = d.record_type;
+  p->fused = pl.fused_combine != 0;
   // alignment the chosen kernel's copies need (TMA boxes, 16-byte loads and stores)
   bool aligned = true;
   switch (pl.kernel) {
@@ -435,7 +447,7 @@ tllm_status tllm_decode_attn_combine(const void* q, const void* k_cache, const v
   tllm_status st = make_params(q, k_cache, v_cache, block_table, context_lens, query_len, kv_scales, sinks, window,
                                num_splits, workspace, out, &p);
   if (st != TLLM_OK) return st;
-  if (num_splits <= 1) return TLLM_OK;
+  if (num_splits <= 1 || p.fused) return TLLM_OK;     // fused: the partial kernel merged
   return launch_combine(p, (cudaStream_t)stream) == cudaSuccess ? TLLM_OK : TLLM_ERR_CUDA;
 }
 
@@ -448,7 +460,7 @@ tllm_status tllm_decode_attn_splitkv(const void* q, const void* k_cache, const v
                                num_splits, workspace, out, &p);
   if (st != TLLM_OK) return st;
   st = run_partial(p, workspace->plan->kernel, (cudaStream_t)stream);
-  if (st != TLLM_OK || num_splits <= 1) return st;
+  if (st != TLLM_OK || num_splits <= 1 || p.fused) return st;
   return launch_combine(p, (cudaStream_t)stream) == cudaSuccess ? TLLM_OK : TLLM_ERR_CUDA;
 }
 
@@ -458,7 +470,10 @@ tllm_status tllm_decode_attn_read_status(const tllm_workspace* ws, uint32_t* fla
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, ws->ptr, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return TLLM_ERR_CUDA;
-  if (reset && cudaMemsetAsync(ws->ptr, 0, sizeof(uint32_t), s) != cudaSuccess) return TLLM_ERR_CUDA;
+  // reset: the status word, and with a plan the arrival counters of the fused combine too
+  const size_t clear = ws->plan ? header_bytes(ws->plan->batch, ws->plan->desc.num_kv_heads) : sizeof(uint32_t);
+  if (reset && cudaMemsetAsync(ws->ptr, 0, clear <= ws->bytes ? clear : sizeof(uint32_t), s) != cudaSuccess)
+    return TLLM_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return TLLM_ERR_CUDA;
   *flags = v;
   return TLLM_OK;

@@ -29,6 +29,7 @@ struct Params {
   const float* sinks;               // [Hq] or nullptr
   void* out;
   uint32_t* status;                 // workspace status word
+  uint32_t* counters;               // [B*Hkv] arrival counters of the fused combine
   float* ws_lse;                    // [B*Hkv][max_splits][R]
   float* ws_o;                      // [B*Hkv][max_splits][R][D] in rec_type (fp32, or 16-bit viewed through it)
   int B, Lq, Hq, Hkv, G, D, R, bs;
@@ -38,6 +39,7 @@ struct Params {
   int q_dtype, kv_dtype, out_dtype;
   int v_dim_major;                  // v_cache [num_pages, Hkv, D, bs] (TLLM_V_DIM_MAJOR)
   int rec_type;                     // tllm_record_type of the split records
+  int fused;                        // the partial kernel merges the splits (no combine launch)
 };
 
 // Element i of the split-record area: fp32, or bf16 / f16 when the plan asked for 16-bit records.
@@ -256,6 +258,77 @@ __device__ __forceinline__ void store_f32(void* base, int dtype, int64_t i, floa
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2half_rn(v); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---- the fused combine -----------------------------------------------------------------
+// Record element i, read through L2 (written by other CTAs of the same launch).
+__device__ __forceinline__ float load_rec(const Params& p, int64_t i) {
+  if (p.rec_type == TLLM_RECORD_F32) return __ldcg(p.ws_o + i);
+  const unsigned short h = __ldcg(reinterpret_cast<const unsigned short*>(p.ws_o) + i);
+  return p.rec_type == TLLM_RECORD_BF16 ? __uint_as_float((uint32_t)h << 16)
+                                        : __half2float(__ushort_as_half(h));
+}
+
+// One CTA merges the n split records of unit u (request b, kv head g) into the output: per
+// packed row the max-LSE-stabilised weighted sum over the splits in split order, with the sink
+// once in the denominator, rows that saw no key zero; the same arithmetic as the combine kernel
+// ("split-KV decode attention design record", tiny-llm PR #11, open question 1: the last CTA
+// of a request merges its partials; "split packed-Q8 verifier KV scans", hipfire PR #760,
+// Summary: stable max-LSE merge). Every thread of the CTA calls it. `wsm` is shared scratch of
+// at least n * R floats: the LSEs are read once into it and turned into normalised weights per
+// row, then every output element loads all its records at once (their latencies overlap).
+__device__ __forceinline__ void merge_unit(const Params& p, int u, int b, int g, int n, float* wsm) {
+  const int D = p.D, R = p.R;
+  const float* lse = p.ws_lse + (int64_t)u * p.max_splits * R;
+  for (int i = threadIdx.x; i < n * R; i += blockDim.x) wsm[i] = __ldcg(lse + i);   // [s][r]
+  __syncthreads();
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int s = 0; s < n; s++) M = fmaxf(M, wsm[s * R + r]);
+    float den = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < n; s++) den += exp2f(wsm[s * R + r] - M);   // 0 for a split with no key
+      if (p.sinks) {
+        const float sk = p.sinks[g * p.G + r % p.G] * kLog2e, M2 = fmaxf(M, sk);
+        den = den * exp2f(M - M2) + exp2f(sk - M2);
+        M = M2;
+      }
+    }
+    for (int s = 0; s < n; s++) wsm[s * R + r] = M == -INFINITY ? 0.f : exp2f(wsm[s * R + r] - M) / den;
+  }
+  __syncthreads();
+  const int64_t rec0 = (int64_t)u * p.max_splits * R * D;
+  for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+    const int r = idx / D, d = idx % D;
+    float acc = 0.f;
+    for (int s0 = 0; s0 < n; s0 += 8) {
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++)
+        x[k] = s0 + k < n && wsm[(s0 + k) * R + r] != 0.f ? load_rec(p, rec0 + ((int64_t)(s0 + k) * R + r) * D + d) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; k++)
+        if (s0 + k < n) acc = fmaf(wsm[(s0 + k) * R + r], x[k], acc);
+    }
+    store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + r / p.G) * p.Hq + g * p.G + r % p.G) * D + d, acc);
+  }
+}
+
+// Called by every thread of a CTA that has just written the split record of unit u (stores
+// issued, not yet fenced): the CTA whose record completes the request's n records (an arrival
+// ticket on the unit's counter, which wraps back to zero on that last arrival, so nothing
+// waits and the counter is ready for the next call) merges them. `flag` is a shared int, `wsm`
+// shared scratch of n * R floats.
+__device__ __forceinline__ void fused_combine_arrive(const Params& p, int u, int b, int g, int n, int* flag,
+                                                     float* wsm) {
+  __threadfence();                                   // this CTA's records, visible GPU-wide
+  __syncthreads();
+  if (threadIdx.x == 0) *flag = atomicInc(p.counters + u, (unsigned)(n - 1)) == (unsigned)(n - 1);
+  __syncthreads();
+  if (*flag) {
+    __threadfence();                                 // every other record, seen after the ticket
+    merge_unit(p, u, b, g, n, wsm);
+  }
+}
 
 // Programmatic dependent launch: a partial kernel lets the combine grid be scheduled as soon
 // as all its CTAs have started (the combine's CTAs then sit on free SM slots, so its launch

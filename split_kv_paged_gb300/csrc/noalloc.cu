@@ -71,8 +71,10 @@ extern "C" tllm_status tllm_decode_attn_splitkv_noalloc(const void* q, const voi
   st = scratch_address(&scratch);
   if (st != TLLM_OK) return st;
   ws.ptr = scratch;
-  // The status word at the head of the records starts each call at zero.
-  if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess) return TLLM_ERR_CUDA;
+  // The header (status word and the fused combine's arrival counters) starts each call at zero.
+  size_t lse_off = 0;
+  tllm_decode_attn_workspace_layout(plan, nullptr, &lse_off, nullptr);
+  if (cudaMemsetAsync(scratch, 0, lse_off, (cudaStream_t)stream) != cudaSuccess) return TLLM_ERR_CUDA;
   return tllm_decode_attn_splitkv(q, k_cache, v_cache, block_table, context_lens, query_len, kv_scales, sinks,
                                   window, num_splits, &ws, out, stream);
 }

@@ -159,6 +159,7 @@ struct Shape {
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static_assert(kTpg >= 1 && kTile % kGroups == 0, "tile");
+  static_assert(kRingBytes >= kMaxSplits * 8 * 4, "the fused merge's weights (splits x rows) fit in the ring");
   static_assert(kTile * kChunksPerRow % kThreads == 0, "copy split");
 };
 
@@ -422,6 +423,12 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
       store_rec(p, ((int64_t)u_split * p.R + r) * D + d, L > 0.f ? O / L : 0.f);
       if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
+  }
+  // fused combine: the CTA that completes the request's records merges them into the output
+  if (!finalize && p.fused) {
+    __shared__ int last_arrival;
+    __syncthreads();                                       // the merge area below is free again
+    fused_combine_arrive(p, u, b, g, sp.nsplit, &last_arrival, reinterpret_cast<float*>(smem));
   }
 }
 

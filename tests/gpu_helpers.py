@@ -31,10 +31,12 @@ def plan_for(wl, kernel=B.TLLM_KERNEL_AUTO, splits=0, host_ctx=None, num_pages=N
 
 
 def poisoned_workspace(plan) -> B.Workspace:
+    """A workspace whose split-record areas hold NaN bytes; its header (status word and the
+    fused combine's arrival counters) is zero, as the C ABI asks before a first call."""
     ws = B.Workspace(plan)
     ws.buffer.fill_(NAN_BYTE)
-    so, _, _ = B.tllm_decode_attn_workspace_layout(plan)
-    ws.buffer[so:so + 4].zero_()
+    _, lo, _ = B.tllm_decode_attn_workspace_layout(plan)
+    ws.buffer[:lo].zero_()
     return ws
 
 

@@ -325,3 +325,26 @@ def test_sixteen_bit_records_halve_the_record_area(lib):
     _, lo16, oo16 = B.tllm_decode_attn_workspace_layout(bf16)
     assert (lo16, oo16) == (lo, oo)
     assert abs((bf16.workspace_bytes - oo16) * 2 - o32) <= 512
+
+
+def test_fused_combine_only_when_asked_and_for_small_records(lib):
+    """The fused merge is taken only when the desc asks for it, by the few-row CUDA-core kernel
+    when a request's records are small (the single decode); not for one split, not for the
+    tensor-core kernels' large records, and never by default."""
+    wl = W.single_decode()
+    def plan(w, S=0, mode=B.TLLM_COMBINE_FUSED):
+        return B.tllm_decode_attn_plan(B.desc_for(w, combine_mode=mode), w.B, w.Lq, w.window, host_ctx_lens=w.ctx,
+                                       splits_override=S)
+    assert plan(wl, 4).fused_combine == 1
+    assert plan(wl, 4, B.TLLM_COMBINE_KERNEL).fused_combine == 0
+    assert plan(wl, 1).fused_combine == 0
+    for wl2 in (W.verify16_int8(), W.ragged_fp8(bs=128), W.mtp4_fp8_long()):
+        assert plan(wl2).fused_combine == 0
+        assert _plan(wl2, host_ctx_lens=wl2.ctx).fused_combine == 0
+
+
+def test_workspace_header_holds_one_counter_per_request_and_kv_head(lib):
+    wl = W.window_sink_bf16(batch=64)
+    p = _plan(wl, host_ctx_lens=wl.ctx, splits_override=2)
+    so, lo, oo = B.tllm_decode_attn_workspace_layout(p)
+    assert so == 0 and lo >= 256 + 4 * wl.B * wl.Hkv and lo % 256 == 0

@@ -764,3 +764,44 @@ def test_sixteen_bit_records(wl, seed, rec):
         plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
         out, _, _ = run_gpu(inp, plan=plan)
         assert_close(out, ref, wl.kv_dtype, f"{wl.name} records {rec} S={plan.num_splits}")
+
+
+# --- fused combine (the last CTA of a request merges) -------------------------------------
+
+def test_fused_combine_single_decode():
+    """The single decode at S = 4 and 8 with the fused combine asked for: the CTA that writes a
+    request's last split record merges them (tiny-llm PR #11, open question 1), no combine launch. The
+    partial entry point alone then gives the final output, the counters are back at zero after
+    every call, repeated calls are bit-identical, and the result matches the oracle."""
+    wl = W.single_decode().replace(extra_pages=8)
+    inp = _inputs(wl, 1001)
+    ref, _ = oracle_out(inp)
+    for S in (4, 8):
+        desc = B.desc_for(wl, num_pages=inp.num_pages, combine_mode=B.TLLM_COMBINE_FUSED)
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        assert plan.kernel == B.TLLM_KERNEL_SIMT and plan.fused_combine == 1
+        ws = poisoned_workspace(plan)
+        outs = []
+        for rep in range(3):
+            out = new_out(wl)
+            B.tllm_decode_attn_partial(inp.q, inp.k_cache, inp.v_cache, inp.block_table, inp.context_lens, wl.Lq,
+                                       inp.kv_scales, inp.sinks, wl.window, S, ws, out)
+            torch.cuda.synchronize()
+            _, lo, _ = B.tllm_decode_attn_workspace_layout(plan)
+            assert int(ws.buffer[256:lo].view(torch.int32).abs().sum()) == 0, "counters not back at zero"
+            assert_close(out, ref, wl.kv_dtype, f"fused S{S} rep{rep}")
+            outs.append(out)
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_fused_combine_with_window_sinks_and_empty_rows():
+    wl = W.window_sink_bf16(batch=6).replace(ctx=[9000, 4097, 300, 2, 1, 0], Hq=8, Hkv=2, window=333,
+                                             extra_pages=2)
+    inp = _inputs(wl, 211)
+    ref, _ = oracle_out(inp)
+    desc = B.desc_for(wl, B.TLLM_KERNEL_SIMT, num_pages=inp.num_pages, combine_mode=B.TLLM_COMBINE_FUSED)
+    plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=5)
+    assert plan.fused_combine == 1
+    out, _, _ = run_gpu(inp, plan=plan)
+    assert_close(out, ref, wl.kv_dtype, "fused window + sinks")
+    assert out[5].float().abs().max() == 0
