@@ -1,11 +1,13 @@
-// INT8 tensor-core split-KV partial kernel for sm_103a (tcgen05 kind::f16): int8 KV with
-// per-token fp32 K and V scales, bf16 or f16 Q, head_dim 128 or 256, up to 128 packed rows per
-// KV head (GQA groups x query rows: the speculative-verify shape), block size 8..128.
+// Widening tensor-core split-KV partial kernel for sm_103a (tcgen05 kind::f16): int8 or FP8
+// e4m3 KV with per-token fp32 K and V scales, bf16 or f16 Q, head_dim 64, 128 or 256, up to
+// 128 packed rows per KV head (GQA groups x query rows: the speculative-verify shape), block
+// size 8..128.
 //
-// Every int8 value is exact in f16, so the cache is widened to f16 in shared memory (a byte
-// permute and one packed subtraction per two values) and both contractions run on the 16-bit
-// tensor cores in f16; the scales stay outside them (the K scale multiplies the score column,
-// the V scale the probability column). A bf16 Q row enters as f16 after a power-of-two scale
+// Every int8 and every e4m3 value is exact in f16, so the cache is widened to f16 in shared
+// memory (int8: a byte permute and one packed subtraction per two values; e4m3: one packed
+// conversion per two values) and both contractions run on the 16-bit tensor cores in f16; the
+// scales stay outside them (the K scale multiplies the score column, the V scale the
+// probability column). A bf16 Q row enters as f16 after a power-of-two scale
 // that is undone on the scores.
 //
 // Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
@@ -75,7 +77,7 @@ struct Lay {
   static constexpr uint32_t kSmem = kOffList + kListWords * 4 + 1024;   // + alignment slack
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(kOff16 % 1024 == 0 && kOffP % 1024 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0, "alignment");
-  static_assert(8 * 32 * kEpiStride * 4 <= kStages8 * kStage8, "output staging fits in the int8 ring");
+  static_assert(8 * 32 * kEpiStride * 4 <= kOffP, "output staging fits in the staging ring and f16 stage");
 };
 
 // mbarriers (8 bytes each), named by their shared-memory address. The one f16 stage has a K
@@ -117,7 +119,8 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-template <int D>
+// kE4m3: the cache holds FP8 e4m3 codes instead of int8
+template <int D, bool kE4m3>
 __global__ void __launch_bounds__(kThreads)
     partial_tc_i8_kernel(const Params p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
@@ -336,6 +339,7 @@ __global__ void __launch_bounds__(kThreads)
       // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
       if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
         set_abort_i8(abort, p.status);
+      const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + 2 * kT * D + S::kSc);
       uint4 w[kPer];
 #pragma unroll
       for (int i = 0; i < kPer; i++) {
@@ -345,14 +349,30 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int i = 0; i < kPer; i++) {
         const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
-        const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
-                                w[i].w ^ 0x80808080u};
         uint32_t h[8];
+        if constexpr (kE4m3) {
+          // two e4m3 codes -> f16x2, element 0 (the lower byte) in the low half. A V token this
+          // split does not read (a slot past the context, before the window, or of a page not
+          // loaded) becomes zero: an e4m3 code can be NaN, and the PV MMA would carry 0 x NaN.
+          // (K needs no such care: the softmax selects -inf for those tokens' scores.)
+          const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+          bool ok = true;
+          if (which == 1) {
+            const int tok = t0 + j * kT + t;
+            const int slot = bs < kT ? t >> bs_sh : 0;
+            ok = ((pmask8 >> slot) & 1) && tok >= vlo && tok < t1;
+          }
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-          const uint32_t x = __byte_perm(ws[e >> 1], 0x64646464u, (e & 1) ? 0x5342u : 0x5140u);
-          const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-          h[e] = *reinterpret_cast<const uint32_t*>(&v2);
+          for (int e = 0; e < 8; e++) h[e] = ok ? e4m3x2_to_f16x2((uint16_t)(ws[e >> 1] >> (16 * (e & 1)))) : 0u;
+        } else {
+          const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
+                                  w[i].w ^ 0x80808080u};
+#pragma unroll
+          for (int e = 0; e < 8; e++) {
+            const uint32_t x = __byte_perm(ws[e >> 1], 0x64646464u, (e & 1) ? 0x5342u : 0x5140u);
+            const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+            h[e] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
         }
         const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
         const uint32_t byte = (d0 & 63) * 2;
@@ -422,10 +442,13 @@ __global__ void __launch_bounds__(kThreads)
         qscale = __int_as_float((127 - e) << 23);
       }
 #pragma unroll
-      for (int c0 = 0; c0 < D / 4; c0 += 32) {
-        uint32_t w[32];
+      // this thread's D / 4 TMEM columns, 32 (or, for head_dim 64, 16) at a time
+      constexpr int kQc = D / 4 < 32 ? D / 4 : 32;
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
+      for (int c0 = 0; c0 < D / 4; c0 += kQc) {
+        uint32_t w[kQc];
+#pragma unroll
+        for (int c = 0; c < kQc / 4; c++) {
           const uint4 x = qv[c0 / 4 + c];
           w[4 * c] = x.x;
           w[4 * c + 1] = x.y;
@@ -434,13 +457,14 @@ __global__ void __launch_bounds__(kThreads)
         }
         if (qbf) {
 #pragma unroll
-          for (int k = 0; k < 32; k++) {
+          for (int k = 0; k < kQc; k++) {
             const __half2 h2 = __floats2half2_rn(__uint_as_float(w[k] << 16) * emul,
                                                  __uint_as_float(w[k] & 0xffff0000u) * emul);
             w[k] = *reinterpret_cast<const uint32_t*>(&h2);
           }
         }
-        tmem_st32(tmem + lane_off + kColQ + hh * (D / 4) + c0, w);
+        if constexpr (kQc == 32) tmem_st32(tmem + lane_off + kColQ + hh * (D / 4) + c0, w);
+        else tmem_st16(tmem + lane_off + kColQ + hh * (D / 4) + c0, w);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -608,8 +632,8 @@ __global__ void __launch_bounds__(kThreads)
     }
     // O leaves through shared memory, 32 columns at a time: a thread holds one row, so storing
     // from registers would touch 32 rows per instruction; staged, each warp stores its own 32
-    // rows as whole 128-byte lines. The int8 staging ring is free here: every tile's copies
-    // landed and were widened before its PV.
+    // rows as whole 128-byte lines. The staging ring and the f16 stage are free here: every
+    // tile's copies landed and were widened before its PV, and its MMAs are done.
     float* stage = reinterpret_cast<float*>(sm + S::kOff8) + (warp - 4) * 32 * kEpiStride;
     const bool keep = !ld_volatile_shared(abort);
     // output row offset of this lane's row (-1: padding), computed once and shuffled to the
@@ -714,7 +738,7 @@ bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int D, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kE4m3>
 cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   CUtensorMap km, vm;
   const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.bs;
@@ -722,22 +746,32 @@ cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows) || !encode_i8_map(&vm, p.v_cache, rows, D, box_rows))
     return cudaErrorInvalidValue;
   constexpr int smem = (int)Lay<D>::kSmem;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D>), smem);
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kE4m3>), smem);
   if (e != cudaSuccess) return e;
   const int n_items = p.B * p.Hkv * p.num_splits;
   const int n_sm = sm_count();
   if (n_sm <= 0) return cudaErrorInvalidValue;
   dim3 grid(n_items < n_sm ? n_items : n_sm);
-  partial_tc_i8_kernel<D><<<grid, kThreads, smem, stream>>>(p, km, vm);
+  partial_tc_i8_kernel<D, kE4m3><<<grid, kThreads, smem, stream>>>(p, km, vm);
   return cudaGetLastError();
+}
+
+template <bool kE4m3>
+cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 64: return launch_d<64, kE4m3>(p, stream);
+    case 128: return launch_d<128, kE4m3>(p, stream);
+    case 256: return launch_d<256, kE4m3>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
-  return d.kv_dtype == TLLM_INT8 && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) && (d.head_dim == 128 || d.head_dim == 256) &&
-         d.v_layout == TLLM_V_TOKEN_MAJOR &&
+  return (d.kv_dtype == TLLM_INT8 || d.kv_dtype == TLLM_FP8_E4M3) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
+         (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) && d.v_layout == TLLM_V_TOKEN_MAJOR &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
 }
@@ -748,7 +782,7 @@ bool tc_i8_pointers_ok(const Params& p) {
 }
 
 cudaError_t launch_partial_tc_i8(const Params& p, cudaStream_t stream) {
-  return p.D == 256 ? launch_d<256>(p, stream) : launch_d<128>(p, stream);
+  return p.kv_dtype == TLLM_FP8_E4M3 ? launch_kv<true>(p, stream) : launch_kv<false>(p, stream);
 }
 
 }  // namespace tllm

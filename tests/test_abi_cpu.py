@@ -348,3 +348,18 @@ def test_workspace_header_holds_one_counter_per_request_and_kv_head(lib):
     p = _plan(wl, host_ctx_lens=wl.ctx, splits_override=2)
     so, lo, oo = B.tllm_decode_attn_workspace_layout(p)
     assert so == 0 and lo >= 256 + 4 * wl.B * wl.Hkv and lo % 256 == 0
+
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "i8"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_auto_never_falls_back_for_quantised_caches(lib, kv, D):
+    """FP8 and INT8 caches with a 16-bit query: for every head_dim and up to 128 packed rows,
+    AUTO picks a tensor-core kernel (or the pipelined CUDA-core kernel for at most 8 rows),
+    never the generic kernel."""
+    for G, Lq in ((1, 1), (7, 1), (4, 4), (8, 4), (16, 4), (24, 4), (6, 16), (8, 16)):
+        wl = W.mtp4_fp8_long(batch=2, ctx=1000).replace(Hq=G, Hkv=1, Lq=Lq, D=D, kv_dtype=kv, q_dtype="bf16")
+        k = _plan(wl, host_ctx_lens=wl.ctx).kernel
+        assert k != B.TLLM_KERNEL_GENERIC, (kv, D, G * Lq)
+        if G * Lq > 8:
+            assert k in (B.TLLM_KERNEL_TC_FP8, B.TLLM_KERNEL_TC_I8), (kv, D, G * Lq, k)

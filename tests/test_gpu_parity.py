@@ -805,3 +805,33 @@ def test_fused_combine_with_window_sinks_and_empty_rows():
     out, _, _ = run_gpu(inp, plan=plan)
     assert_close(out, ref, wl.kv_dtype, "fused window + sinks")
     assert out[5].float().abs().max() == 0
+
+
+
+# --- the widening kernel on FP8 e4m3 caches and head_dim 64 ------------------------------
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv,Lq", [(24, 4, 16), (8, 1, 16), (16, 1, 8)])
+def test_widening_kernel_fp8_cache(Hq, Hkv, Lq, D):
+    """FP8 e4m3 caches widened to f16 (exact) by the same kernel that widens int8, at every
+    head_dim: the shapes the FP8 tensor-core kernel does not take (head_dim 64 / 256, or more
+    than 64 packed rows), with a window, sinks and ragged lengths."""
+    wl = W.mtp4_fp8_long(batch=3, ctx=1).replace(ctx=[3000, 700, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, window=900,
+                                                 sinks=True, extra_pages=4)
+    inp = _inputs(wl, 220 + D + Hq)
+    ref, _ = oracle_out(inp)
+    for S in (1, 3):
+        out, plan, _ = run_gpu(inp, TCI8, splits=S)
+        assert plan.kernel == TCI8
+        assert_close(out, ref, wl.kv_dtype, f"widening e4m3 Hq{Hq} Hkv{Hkv} Lq{Lq} D{D} S{S}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,Lq", [(24, 4, 16), (4, 4, 4), (32, 1, 4)])
+def test_widening_kernel_int8_head_dim_64(Hq, Hkv, Lq):
+    wl = W.verify16_int8().replace(ctx=[3000, 700, 65, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=64, extra_pages=4)
+    inp = _inputs(wl, 230 + Hq)
+    ref, _ = oracle_out(inp)
+    for S in (1, 3):
+        out, plan, _ = run_gpu(inp, TCI8, splits=S)
+        assert plan.kernel == TCI8
+        assert_close(out, ref, wl.kv_dtype, f"widening int8 D64 Hq{Hq} Hkv{Hkv} Lq{Lq} S{S}")
