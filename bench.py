@@ -477,6 +477,7 @@ def main():
             and args.batch == 0 and args.ctx == 0 and args.bs == 0:
         k_o, w_o = args.other_steps, max(3, min(args.warmup, 5))
         specs = [("single_decode_S1", W.single_decode(), 1001, 1), ("single_decode_S4", W.single_decode(), 1001, 4),
+                 ("single_decode", W.single_decode(), 1001, 0),
                  ("verify16_int8", W.verify16_int8(), 1002, 0),
                  ("ragged_fp8_bs128", W.ragged_fp8(bs=128), 1004, 0),
                  ("ragged_fp8_bs16", W.ragged_fp8(bs=16), 1004, 0),

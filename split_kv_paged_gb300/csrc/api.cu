@@ -181,7 +181,7 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
   const KernelTraits kt = traits(kernel, d, rows);
   const int max_ctx = d.max_blocks_per_seq * d.block_size;
   const int align = split_align(kt, d.block_size);
-  const int min_chunk = ((256 + align - 1) / align) * align;
+  const int min_chunk = align;                 // smallest split: one tile (or one page when pages are larger)
   if (num_sms <= 0) num_sms = 152;
 
   // Lengths the plan should fit: the host copy, else the hints (one request at the

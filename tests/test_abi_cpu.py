@@ -225,7 +225,7 @@ def test_tensor_core_kernels_reject_misaligned_pointers(lib, wl, field):
     (W.mtp4_fp8_long(), 3),            # 600 items on 152 SMs: four even waves
     (W.ragged_fp8(bs=128), 131),       # 12-tile splits: 131 of the 200k request + 15 short, one wave
     (W.verify16_int8(), 36),
-    (W.single_decode(), 8),
+    (W.single_decode(), 32),           # one 64-token tile per split: 64 CTAs, all in one wave
     (W.window_sink_bf16(), 1),         # HBM-bound 16-bit kernel: no split, no combine
 ])
 def test_planner_choices_on_the_measured_workloads(lib, wl, S):
