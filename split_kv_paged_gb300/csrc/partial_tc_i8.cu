@@ -1,13 +1,17 @@
 // Widening tensor-core split-KV partial kernel for sm_103a (tcgen05 kind::f16): int8 or FP8
-// e4m3 KV with per-token fp32 K and V scales, bf16 or f16 Q, head_dim 64, 128 or 256, up to
-// 128 packed rows per KV head (GQA groups x query rows: the speculative-verify shape), block
-// size 8..128.
+// e4m3 KV with per-token fp32 K and V scales (head_dim 64, 128 or 256), or f16 / bf16 KV (head_dim
+// 64 or 128); bf16 or f16 Q; up to 128 packed rows per KV head (GQA groups x query rows: the
+// speculative-verify shape); block size 8..128.
 //
 // Every int8 and every e4m3 value is exact in f16, so the cache is widened to f16 in shared
 // memory (int8: a byte permute and one packed subtraction per two values; e4m3: one packed
 // conversion per two values) and both contractions run on the 16-bit tensor cores in f16; the
 // scales stay outside them (the K scale multiplies the score column, the V scale the
-// probability column). A bf16 Q row enters as f16 after a power-of-two scale
+// probability column). An f16 cache is copied as it is. A bf16 K tile enters f16 scaled by a
+// power of two chosen from its largest value, which then stands as the tile's per-token scale;
+// a bf16 V tile stays bf16, and the PV contraction runs in bf16 with P sent as a high part
+// plus the bf16 rounding of its remainder (about 16 significant bits of P), so V keeps bf16's
+// whole range. A bf16 Q row enters as f16 after a power-of-two scale
 // that is undone on the scores.
 //
 // Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
@@ -60,18 +64,24 @@ constexpr int kSmThreads = 256;         // softmax: 8 warps, two threads per TME
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-template <int D>
+// Cache element types the kernel widens: int8 and e4m3 (exact in f16, per-token scales), f16
+// (copied) and bf16 (scaled into f16 by a power of two per tile).
+constexpr int kKvI8 = 0, kKvE4m3 = 1, kKvF16 = 2, kKvBf16 = 3;
+
+template <int D, int kEsz, int kPParts>
 struct Lay {
   static constexpr uint32_t kAtom = kT * 128;                 // bytes of one atom column of a tile
   static constexpr uint32_t kSc = 2 * kT * 4;                 // K scales | V scales
   static constexpr uint32_t kMeta = kSc + 16;                 // scales | page mask | largest V scale x2
-  static constexpr uint32_t kStage8 = align1k(2 * kT * D + kSc + 16);  // int8 K | V | scales | mask
+  static constexpr uint32_t kRaw = kT * D * kEsz;             // one staged operand tile (K or V) as stored
+  static constexpr uint32_t kStage8 = align1k(2 * kRaw + kSc + 16);    // K | V | scales | mask, as stored
   static constexpr uint32_t kHalf16 = kT * D * 2;                      // one f16 tile (K or V)
   static constexpr uint32_t kOff8 = 0, kOff16 = kStages8 * kStage8, kOffP = kOff16 + 2 * kHalf16;
-  static constexpr uint32_t kPBuf = 128 * 128;                // P: 128 rows x 64 tokens f16
+  static constexpr uint32_t kPPart = 128 * 128;               // P: 128 rows x 64 tokens, 16-bit
+  static constexpr uint32_t kPBuf = kPPart * kPParts;         // (bf16 V: high part | low part)
   static constexpr uint32_t kOffMeta = kOffP + 2 * kPBuf;     // meta ring: 4 tiles
   static constexpr uint32_t kOffX = kOffMeta + 4 * kMeta;     // exchange floats (see xf below)
-  static constexpr uint32_t kOffBar = kOffX + 8 * 128 * 4;
+  static constexpr uint32_t kOffBar = kOffX + 8 * 128 * 4 + 64;
   static constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
   static constexpr uint32_t kOffList = kOffMisc + 64;         // work list + its scan scratch
   static constexpr uint32_t kSmem = kOffList + kListWords * 4 + 1024;   // + alignment slack
@@ -119,12 +129,15 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// kE4m3: the cache holds FP8 e4m3 codes instead of int8
-template <int D, bool kE4m3>
+// kKv: the cache's element type (kKvI8, kKvE4m3, kKvF16 or kKvBf16)
+template <int D, int kKv>
 __global__ void __launch_bounds__(kThreads)
     partial_tc_i8_kernel(const Params p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
-  using S = Lay<D>;
+  constexpr bool k16 = kKv == kKvF16 || kKv == kKvBf16;   // 16-bit cache: no per-token scales
+  constexpr int kEsz = k16 ? 2 : 1;
+  constexpr int kPParts = kKv == kKvBf16 ? 2 : 1;          // bf16 V: P as high + low bf16 parts
+  using S = Lay<D, kEsz, kPParts>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(sm);
@@ -143,7 +156,8 @@ __global__ void __launch_bounds__(kThreads)
   const int brows = bs < kT ? bs : kT;                     // rows of one TMA box
   const int ppt = bs < kT ? kT >> bs_sh : 1;               // pages a tile touches
   // exchange floats of the two threads of a row: [0, 512) tile row maxima [parity][half][row],
-  // [512, 768) query maxima [half][row], [768, 1024) row sums [half][row]
+  // [512, 768) query maxima [half][row], [768, 1024) row sums [half][row]; [1024, 1026) the K
+  // converter warps' tile maxima (bf16 K)
   float* xf = reinterpret_cast<float*>(sm + S::kOffX);
 
   // the real (request x kv head, split) items of the work list, in turn
@@ -228,26 +242,29 @@ __global__ void __launch_bounds__(kThreads)
       const int tt = t0 + j * kT;
       const uint32_t mask = __ballot_sync(kFull, pg >= 0);
       const uint32_t stg = sbase + S::kOff8 + st * S::kStage8;
-      if (lane == 0) mbar_arrive_expect_tx(bars.full8(st), __popc(mask) * (uint32_t)brows * D * 2);
+      if (lane == 0) mbar_arrive_expect_tx(bars.full8(st), __popc(mask) * (uint32_t)brows * D * 2 * kEsz);
       __syncwarp();
       if (pg >= 0) {
         const int row = (int)(((int64_t)pg * p.Hkv + g) * bs + (bs > kT ? (tt & (bs - 1)) : 0));
-        tma_load_2d(stg + lane * brows * D, &kmap, 0, row, bars.full8(st));
-        tma_load_2d(stg + kT * D + lane * brows * D, &vmap, 0, row, bars.full8(st));
+        tma_load_2d(stg + lane * brows * D * kEsz, &kmap, 0, row, bars.full8(st));
+        tma_load_2d(stg + S::kRaw + lane * brows * D * kEsz, &vmap, 0, row, bars.full8(st));
       }
-      // scales: lanes 0..15 copy K scales of tokens 4l..4l+3, lanes 16..31 the V scales
+      // scales (quantised caches): lanes 0..15 copy K scales of tokens 4l..4l+3, lanes 16..31
+      // the V scales; every lane arrives once its copy (if any) has landed
       {
-        const int tk = 4 * (lane & 15);
-        const int slot = bs < kT ? tk >> bs_sh : 0;
-        const int pgl = __shfl_sync(kFull, pg, slot);
-        const bool ok = pgl >= 0;
-        const int64_t srow = ok ? ((int64_t)pgl * p.Hkv + g) * bs + ((tt + tk) & (bs - 1)) : 0;
-        const float* src = (lane < 16 ? p.k_scales : p.v_scales) + srow;
-        cp_async16(stg + 2 * kT * D + (lane < 16 ? 0 : kT * 4) + tk * 4, src, ok ? 16u : 0u);
+        if constexpr (!k16) {
+          const int tk = 4 * (lane & 15);
+          const int slot = bs < kT ? tk >> bs_sh : 0;
+          const int pgl = __shfl_sync(kFull, pg, slot);
+          const bool ok = pgl >= 0;
+          const int64_t srow = ok ? ((int64_t)pgl * p.Hkv + g) * bs + ((tt + tk) & (bs - 1)) : 0;
+          const float* src = (lane < 16 ? p.k_scales : p.v_scales) + srow;
+          cp_async16(stg + 2 * S::kRaw + (lane < 16 ? 0 : kT * 4) + tk * 4, src, ok ? 16u : 0u);
+        }
         cp_async_arrive_noinc(bars.full8(st));
       }
       if (lane == 0) {
-        *reinterpret_cast<volatile uint32_t*>(sm + S::kOff8 + st * S::kStage8 + 2 * kT * D + S::kSc) = mask;
+        *reinterpret_cast<volatile uint32_t*>(sm + S::kOff8 + st * S::kStage8 + 2 * S::kRaw + S::kSc) = mask;
         mbar_arrive(bars.full8(st));
       }
       issued = j + 1;
@@ -276,7 +293,7 @@ __global__ void __launch_bounds__(kThreads)
           mma_commit(bars.emptyK());
         }
       } else {
-        const uint32_t idpv = idesc_f16(128, D, 0, 0, 1);   // P and V in f16
+        const uint32_t idpv = idesc_f16(128, D, kPParts - 1, 0, 1);   // P and V in f16 (bf16 V: both bf16)
         const uint32_t vt = sbase + S::kOff16 + S::kHalf16;
         for (int j = 0; ok && j < n_tiles; j++) {
           const int pb = j & 1;
@@ -285,8 +302,11 @@ __global__ void __launch_bounds__(kThreads)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kT / 16; k++)
-            mma_f16_ss(tmem + kColO, sdesc_sw128(sbase + S::kOffP + pb * S::kPBuf + 32 * k, 16, 1024),
-                       sdesc_sw128(vt + 2048 * k, S::kAtom, 1024), idpv, (j > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int part = 0; part < kPParts; part++)
+              mma_f16_ss(tmem + kColO,
+                         sdesc_sw128(sbase + S::kOffP + pb * S::kPBuf + part * S::kPPart + 32 * k, 16, 1024),
+                         sdesc_sw128(vt + 2048 * k, S::kAtom, 1024), idpv, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
           mma_commit(bars.pv_done(pb));
           mma_commit(bars.emptyV());
         }
@@ -300,86 +320,131 @@ __global__ void __launch_bounds__(kThreads)
     // (an aligned barrier) converged
     __syncwarp();
   } else if (warp >= 12) {
-    // ---------------- converters: int8 tile -> f16 tile (exact), scales and mask ----------------
+    // ---------------- converters: a staged tile -> f16 tile, scales and mask ----------------
     // Warps 12, 13 widen K, warps 14, 15 widen V, each pair at its own pace: K(j + 1) waits only
     // for the QK^T of tile j, V(j + 1) only for the PV of tile j.
     const int ct = tid - 384;                              // 0..127
     const int which = ct >> 6;                             // 0: K, 1: V
     const int cw = ct & 63;                                // thread within the pair
+    constexpr int kEpc = 16 / kEsz;                        // elements per 16-byte chunk
+    constexpr int kChunksPerRow = D / kEpc, kPer = kT * kChunksPerRow / 64;
+    float* xc = xf + 1024;                                 // the K pair's tile maxima (bf16 K)
     for (int j = 0; j < n_tiles; j++) {
       const int st = j % kStages8;
       if (!mbar_wait(bars.full8(st), (j / kStages8) & 1, abort)) set_abort_i8(abort, p.status);
       const uint8_t* src = sm + S::kOff8 + st * S::kStage8;
       const uint32_t dst = sbase + S::kOff16;
-      // The tile's meta first, into ring slot j % 4: scales (K by the K pair, V by the V pair),
-      // the page mask and the tile's largest |V scale| (unread pages were zero-filled, and a
-      // non-finite scale is left out). The K scales leave here multiplied by the softmax scale
-      // in log2 units, so that a score reaches the softmax as one product with the query row's
-      // power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax is over:
-      // tile j's copies were issued after both pairs released tile j - 3's stage, and the V pair
-      // widened tile j - 3 only after the PV of tile j - 4, which waited for that softmax.
+      const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + 2 * S::kRaw + S::kSc);
+      const int tt = t0 + j * kT;
+      // is row t of this tile a token the split reads? (a slot past the context, before the
+      // window, or of a page not loaded holds stale or poisoned bytes)
+      auto read_tok = [&](int t) -> bool {
+        const int slot = bs < kT ? t >> bs_sh : 0;
+        return ((pmask8 >> slot) & 1) && tt + t >= vlo && tt + t < t1;
+      };
+      // this thread's chunks of its operand, loaded before anything is converted (their
+      // latencies overlap)
+      uint4 w[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; i++) {
+        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+        w[i] = *reinterpret_cast<const uint4*>(src + which * S::kRaw + (t * D + d0) * kEsz);
+      }
+      // A bf16 K tile enters f16 scaled by 2^e, e from the largest |x| the split reads in it, so
+      // that this maximum lies in [2^13, 2^14): every element within 2^-27 of it converts to a
+      // normal f16 exactly (bf16 keeps 8 significant bits, f16 11); a smaller one rounds by at
+      // most 2^-38 of the maximum, below the fp32 rounding bound of the score it enters. 2^-e
+      // goes to the tile's per-token scales. An f16 tile, and a bf16 V tile, is copied as it is
+      // (e = 0).
+      int e = 0;
+      if (kKv == kKvBf16 && which == 0) {
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPer; i++) {
+          const int t = (cw + 64 * i) / kChunksPerRow;
+          if (read_tok(t)) {
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+              mx = fmax3(mx, fabsf(__uint_as_float(ws[k] << 16)), fabsf(__uint_as_float(ws[k] & 0xffff0000u)));
+          }
+        }
+        mx = warp_max_abs(isfinite(mx) ? mx : 0.f);
+        if (lane == 0) xc[warp - 12] = mx;
+        named_bar(2, 64);                                  // the K pair, warps 12 and 13
+        mx = fmaxf(xc[0], xc[1]);
+        named_bar(2, 64);                                  // both read before the next tile's write
+        if (mx > 0.f) e = min(125, max(-125, 14 - exponent_of(mx)));
+      }
+      // The tile's meta, into ring slot j % 4: scales (K by the K pair, V by the V pair), the
+      // page mask and the tile's largest |V scale|. The K scales leave here multiplied by the
+      // softmax scale in log2 units, so that a score reaches the softmax as one product with the
+      // query row's power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax
+      // is over: tile j's copies were issued after both pairs released tile j - 3's stage, and
+      // the V pair widened tile j - 3 only after the PV of tile j - 4, which waited for that
+      // softmax.
       {
-        const float scv = reinterpret_cast<const float*>(src + 2 * kT * D)[ct];
+        float scv;
+        if constexpr (k16) scv = __int_as_float((127 - e) << 23);    // 2^-e, the same for every token
+        else scv = reinterpret_cast<const float*>(src + 2 * S::kRaw)[ct];
         uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
         reinterpret_cast<float*>(meta)[ct] = ct < kT ? scv * p.scale_log2 : scv;
         const float vm = warp_max_abs(ct >= kT && isfinite(scv) ? scv : 0.f);
-        if (ct == 0)
-          *reinterpret_cast<uint32_t*>(meta + S::kSc) =
-              *reinterpret_cast<const volatile uint32_t*>(src + 2 * kT * D + S::kSc);
+        if (ct == 0) *reinterpret_cast<uint32_t*>(meta + S::kSc) = pmask8;
         if (lane == 0 && ct >= kT) reinterpret_cast<float*>(meta + S::kSc + 4)[(ct - kT) >> 5] = vm;
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
       }
-      // 16-element chunks (rows = tokens, atoms of 64 elements). Each thread loads all its
-      // chunks before converting any, so the loads overlap. int8 -> f16 exactly: the byte, sign
-      // bit flipped, placed under the f16 exponent of 1024 reads 1024 + (x + 128); subtracting
-      // 1152 leaves x.
-      constexpr int kChunksPerRow = D / 16, kPer = kT * kChunksPerRow / 64;
-      const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
       // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
       if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
         set_abort_i8(abort, p.status);
-      const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + 2 * kT * D + S::kSc);
-      uint4 w[kPer];
+      const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
+      const float emul = __int_as_float((e + 127) << 23);
 #pragma unroll
       for (int i = 0; i < kPer; i++) {
-        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
-        w[i] = *reinterpret_cast<const uint4*>(src + which * kT * D + t * D + d0);
-      }
-#pragma unroll
-      for (int i = 0; i < kPer; i++) {
-        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * 16;
-        uint32_t h[8];
-        if constexpr (kE4m3) {
-          // two e4m3 codes -> f16x2, element 0 (the lower byte) in the low half. A V token this
-          // split does not read (a slot past the context, before the window, or of a page not
-          // loaded) becomes zero: an e4m3 code can be NaN, and the PV MMA would carry 0 x NaN.
-          // (K needs no such care: the softmax selects -inf for those tokens' scores.)
-          const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-          bool ok = true;
-          if (which == 1) {
-            const int tok = t0 + j * kT + t;
-            const int slot = bs < kT ? t >> bs_sh : 0;
-            ok = ((pmask8 >> slot) & 1) && tok >= vlo && tok < t1;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; e++) h[e] = ok ? e4m3x2_to_f16x2((uint16_t)(ws[e >> 1] >> (16 * (e & 1)))) : 0u;
-        } else {
-          const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
-                                  w[i].w ^ 0x80808080u};
-#pragma unroll
-          for (int e = 0; e < 8; e++) {
-            const uint32_t x = __byte_perm(ws[e >> 1], 0x64646464u, (e & 1) ? 0x5342u : 0x5140u);
-            const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-            h[e] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
-        }
+        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+        // V rows of tokens the split does not read become zero: their bytes may be NaN (an e4m3
+        // or 16-bit code), and the PV MMA would carry 0 x NaN. (K needs no such care: the
+        // softmax selects -inf for those tokens' scores.) Int8 codes are always finite.
+        const bool ok = kKv == kKvI8 || which == 0 || read_tok(t);
+        const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
         const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
         const uint32_t byte = (d0 & 63) * 2;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
-                     "r"(h[2]), "r"(h[3]));
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
-                     "r"(h[5]), "r"(h[6]), "r"(h[7]));
+        if constexpr (!k16) {
+          uint32_t h[8];
+          if constexpr (kKv == kKvE4m3) {
+            // two e4m3 codes -> f16x2, element 0 (the lower byte) in the low half
+#pragma unroll
+            for (int q = 0; q < 8; q++) h[q] = ok ? e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1)))) : 0u;
+          } else {
+            // int8 -> f16 exactly: the byte, sign bit flipped, placed under the f16 exponent of
+            // 1024 reads 1024 + (x + 128); subtracting 1152 leaves x
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+              const uint32_t x = __byte_perm(ws[q >> 1] ^ 0x80808080u, 0x64646464u, (q & 1) ? 0x5342u : 0x5140u);
+              const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+              h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+            }
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
+                       "r"(h[2]), "r"(h[3]));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
+                       "r"(h[5]), "r"(h[6]), "r"(h[7]));
+        } else {
+          uint32_t h[4];
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            if (kKv == kKvBf16 && which == 0) {
+              const __half2 v2 = __floats2half2_rn(__uint_as_float(ws[q] << 16) * emul,
+                                                   __uint_as_float(ws[q] & 0xffff0000u) * emul);
+              h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+            } else {
+              h[q] = ok ? ws[q] : 0u;
+            }
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
+                       "r"(h[2]), "r"(h[3]));
+        }
       }
       fence_proxy_async();
       __syncwarp();
@@ -561,6 +626,7 @@ __global__ void __launch_bounds__(kThreads)
       const float2 qs2 = make_float2(qscale, qscale), e02 = make_float2(e0, e0);
       float2 ls = make_float2(0.f, 0.f);
       uint32_t pw[16];
+      [[maybe_unused]] uint32_t pl[16];                    // bf16 V: the low parts of P
 #pragma unroll
       for (int i4 = 0; i4 < 8; i4++) {
         const float4 v = vs4[i4];
@@ -572,9 +638,20 @@ __global__ void __launch_bounds__(kThreads)
         ls = fadd2(ls, fadd2(p01, p23));
         const float w0 = p01.x != 0.f ? p01.x * v.x : 0.f, w1 = p01.y != 0.f ? p01.y * v.y : 0.f;
         const float w2 = p23.x != 0.f ? p23.x * v.z : 0.f, w3 = p23.y != 0.f ? p23.y * v.w : 0.f;
-        const __half2 h01 = __floats2half2_rn(w0, w1), h23 = __floats2half2_rn(w2, w3);
-        pw[2 * i4] = *reinterpret_cast<const uint32_t*>(&h01);
-        pw[2 * i4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+        if constexpr (kPParts == 2) {
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(w0, w1), h23 = __floats2bfloat162_rn(w2, w3);
+          const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+          const __nv_bfloat162 l01 = __floats2bfloat162_rn(w0 - f01.x, w1 - f01.y);
+          const __nv_bfloat162 l23 = __floats2bfloat162_rn(w2 - f23.x, w3 - f23.y);
+          pw[2 * i4] = *reinterpret_cast<const uint32_t*>(&h01);
+          pw[2 * i4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+          pl[2 * i4] = *reinterpret_cast<const uint32_t*>(&l01);
+          pl[2 * i4 + 1] = *reinterpret_cast<const uint32_t*>(&l23);
+        } else {
+          const __half2 h01 = __floats2half2_rn(w0, w1), h23 = __floats2half2_rn(w2, w3);
+          pw[2 * i4] = *reinterpret_cast<const uint32_t*>(&h01);
+          pw[2 * i4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+        }
       }
       l = l * factor + (ls.x + ls.y);
       const float prev_M = M;
@@ -584,9 +661,13 @@ __global__ void __launch_bounds__(kThreads)
       if (j >= 2 && !mbar_wait(bars.pv_done(sb), ((j - 2) >> 1) & 1, abort)) set_abort_i8(abort, p.status);
       const uint32_t prow = sbase + S::kOffP + sb * S::kPBuf;
 #pragma unroll
-      for (int c = 0; c < 4; c++)
+      for (int c = 0; c < 4; c++) {
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + swz(r, 64 * hh + 16 * c)),
                      "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3]));
+        if constexpr (kPParts == 2)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + S::kPPart + swz(r, 64 * hh + 16 * c)),
+                       "r"(pl[4 * c]), "r"(pl[4 * c + 1]), "r"(pl[4 * c + 2]), "r"(pl[4 * c + 3]));
+      }
       fence_proxy_async();
       // rescale this row of O (this thread: half of its columns) when its maximum grew or the P
       // scale shrank: O holds the tiles < j, so the PV of tile j - 1 must be done first
@@ -724,44 +805,50 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder_i8() {
   return fn;
 }
 
-// 2-D map over the int8 cache viewed as [pages * Hkv * bs rows][D bytes]; a box is one page
-// (or one 64-token tile of a larger page), unswizzled: the converters read it row by row.
-bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int D, int box_rows) {
+// 2-D map over the cache viewed as [pages * Hkv * bs rows][D elements of esz bytes]; a box is
+// one page (or one 64-token tile of a larger page), unswizzled: the converters read it row by row.
+bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int D, int box_rows, int esz) {
   auto enc = get_encoder_i8();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint64_t strides[1] = {(cuuint64_t)D * esz};
   cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kE4m3>
+template <int D, int kKv>
 cudaError_t launch_d(const Params& p, cudaStream_t stream) {
+  constexpr int kEsz = (kKv == kKvF16 || kKv == kKvBf16) ? 2 : 1;
+  using S = Lay<D, kEsz, kKv == kKvBf16 ? 2 : 1>;
   CUtensorMap km, vm;
   const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.bs;
   const int box_rows = p.bs < kT ? p.bs : kT;
-  if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows) || !encode_i8_map(&vm, p.v_cache, rows, D, box_rows))
+  if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows, kEsz) || !encode_i8_map(&vm, p.v_cache, rows, D, box_rows, kEsz))
     return cudaErrorInvalidValue;
-  constexpr int smem = (int)Lay<D>::kSmem;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kE4m3>), smem);
+  constexpr int smem = (int)S::kSmem;
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kKv>), smem);
   if (e != cudaSuccess) return e;
   const int n_items = p.B * p.Hkv * p.num_splits;
   const int n_sm = sm_count();
   if (n_sm <= 0) return cudaErrorInvalidValue;
   dim3 grid(n_items < n_sm ? n_items : n_sm);
-  partial_tc_i8_kernel<D, kE4m3><<<grid, kThreads, smem, stream>>>(p, km, vm);
+  partial_tc_i8_kernel<D, kKv><<<grid, kThreads, smem, stream>>>(p, km, vm);
   return cudaGetLastError();
 }
 
-template <bool kE4m3>
+template <int kKv>
 cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
   switch (p.D) {
-    case 64: return launch_d<64, kE4m3>(p, stream);
-    case 128: return launch_d<128, kE4m3>(p, stream);
-    case 256: return launch_d<256, kE4m3>(p, stream);
+    case 64: return launch_d<64, kKv>(p, stream);
+    case 128: return launch_d<128, kKv>(p, stream);
+    case 256:
+      // a 16-bit tile of head_dim 256 would not leave room for three staged tiles
+      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv>(p, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -770,19 +857,27 @@ cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
 
 bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
-  return (d.kv_dtype == TLLM_INT8 || d.kv_dtype == TLLM_FP8_E4M3) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
-         (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) && d.v_layout == TLLM_V_TOKEN_MAJOR &&
+  const bool quant = d.kv_dtype == TLLM_INT8 || d.kv_dtype == TLLM_FP8_E4M3;
+  const bool b16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
+  return (quant || b16) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
+         (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && quant)) && d.v_layout == TLLM_V_TOKEN_MAJOR &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
 }
 
 bool tc_i8_pointers_ok(const Params& p) {
   auto al = [](const void* x) { return ((uintptr_t)x & 15) == 0; };
-  return al(p.q) && al(p.k_cache) && al(p.v_cache) && al(p.k_scales) && al(p.v_scales) && al(p.out);
+  const bool quant = p.kv_dtype == TLLM_INT8 || p.kv_dtype == TLLM_FP8_E4M3;
+  return al(p.q) && al(p.k_cache) && al(p.v_cache) && (!quant || (al(p.k_scales) && al(p.v_scales))) && al(p.out);
 }
 
 cudaError_t launch_partial_tc_i8(const Params& p, cudaStream_t stream) {
-  return p.kv_dtype == TLLM_FP8_E4M3 ? launch_kv<true>(p, stream) : launch_kv<false>(p, stream);
+  switch (p.kv_dtype) {
+    case TLLM_FP8_E4M3: return launch_kv<kKvE4m3>(p, stream);
+    case TLLM_F16: return launch_kv<kKvF16>(p, stream);
+    case TLLM_BF16: return launch_kv<kKvBf16>(p, stream);
+    default: return launch_kv<kKvI8>(p, stream);
+  }
 }
 
 }  // namespace tllm

@@ -182,7 +182,8 @@ def test_plan_rejects_bad_call_shape(lib):
     (W.single_decode(), B.TLLM_KERNEL_SIMT),                                             # D 64
     (W.window_sink_bf16().replace(Hq=16, Hkv=1), B.TLLM_KERNEL_TC_B16),                   # 16 rows
     (W.window_sink_bf16().replace(Hq=4, Hkv=1, Lq=4), B.TLLM_KERNEL_TC_B16),              # 16 rows
-    (W.window_sink_bf16().replace(Hq=32, Hkv=1), B.TLLM_KERNEL_GENERIC),                  # 32 rows
+    (W.window_sink_bf16().replace(Hq=32, Hkv=1), B.TLLM_KERNEL_TC_I8),                    # 32 rows
+    (W.window_sink_bf16().replace(Hq=32, Hkv=1, D=256), B.TLLM_KERNEL_GENERIC),           # 32 rows, D 256
     (W.window_sink_bf16().replace(kv_dtype="f16"), B.TLLM_KERNEL_SIMT),                   # bf16 Q, f16 KV
     (W.window_sink_bf16().replace(q_dtype="f16", kv_dtype="f16", out_dtype="f16"), B.TLLM_KERNEL_TC_B16),
     (W.window_sink_bf16().replace(D=256), B.TLLM_KERNEL_SIMT),
@@ -190,7 +191,8 @@ def test_plan_rejects_bad_call_shape(lib):
 def test_auto_kernel_choice(lib, wl, kernel):
     """AUTO takes the FP8 tensor-core kernel for e4m3 KV at head_dim 128, the 16-bit one for
     f16/bf16 KV with a query of the same type, head_dim 128 and at most 16 packed rows, the
-    INT8 one for int8 KV with more than 8 rows, then the CUDA-core kernels."""
+    widening one for int8 KV, and for other 16-bit shapes up to head_dim 128, with more than 8
+    rows, then the CUDA-core kernels."""
     p = _plan(wl, host_ctx_lens=wl.ctx)
     assert p.kernel == kernel
 
@@ -363,3 +365,21 @@ def test_auto_never_falls_back_for_quantised_caches(lib, kv, D):
         assert k != B.TLLM_KERNEL_GENERIC, (kv, D, G * Lq)
         if G * Lq > 8:
             assert k in (B.TLLM_KERNEL_TC_FP8, B.TLLM_KERNEL_TC_I8), (kv, D, G * Lq, k)
+
+
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("f16", "f16"), ("f16", "bf16"), ("bf16", "f16")])
+@pytest.mark.parametrize("D", [64, 128])
+def test_auto_never_falls_back_for_16bit_caches(lib, kv, q, D):
+    """f16 and bf16 caches at head_dim 64 and 128, up to 128 packed rows, with the query of
+    either 16-bit type: AUTO picks a tensor-core kernel (or the pipelined CUDA-core kernel for at
+    most 8 rows), never the generic kernel; the 16-bit tensor-core kernel keeps the shapes it
+    takes (same query and cache type, head_dim 128, at most 16 rows)."""
+    for G, Lq in ((1, 1), (7, 1), (4, 4), (8, 2), (8, 4), (24, 4), (6, 16), (8, 16)):
+        wl = W.window_sink_bf16(batch=2).replace(Hq=G, Hkv=1, Lq=Lq, D=D, kv_dtype=kv, q_dtype=q)
+        k = _plan(wl, host_ctx_lens=wl.ctx).kernel
+        rows = G * Lq
+        assert k != B.TLLM_KERNEL_GENERIC, (kv, q, D, rows)
+        if q == kv and D == 128 and rows <= 16:
+            assert k == B.TLLM_KERNEL_TC_B16, (kv, q, D, rows, k)
+        elif rows > 8:
+            assert k == B.TLLM_KERNEL_TC_I8, (kv, q, D, rows, k)

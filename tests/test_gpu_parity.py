@@ -835,3 +835,72 @@ def test_widening_kernel_int8_head_dim_64(Hq, Hkv, Lq):
         out, plan, _ = run_gpu(inp, TCI8, splits=S)
         assert plan.kernel == TCI8
         assert_close(out, ref, wl.kv_dtype, f"widening int8 D64 Hq{Hq} Hkv{Hkv} Lq{Lq} S{S}")
+
+
+# --- the widening kernel on 16-bit caches ----------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("q_dtype,kv_dtype", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f16"), ("f16", "bf16")])
+@pytest.mark.parametrize("Hq,Hkv,Lq", [(24, 4, 16), (8, 1, 16), (32, 4, 2)])
+def test_widening_kernel_16bit_cache(Hq, Hkv, Lq, q_dtype, kv_dtype, D):
+    """f16 caches copied and bf16 caches scaled into f16 by a power of two per tile: the shapes
+    the 16-bit tensor-core kernel does not take (more than 16 packed rows, head_dim 64, query and
+    cache of different types), with a window, sinks, ragged lengths and poisoned tails."""
+    wl = W.window_sink_bf16(batch=4).replace(ctx=[3000, 700, 65, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, q_dtype=q_dtype,
+                                             kv_dtype=kv_dtype, window=900, bs=16, extra_pages=4)
+    inp = _inputs(wl, 240 + D + Hq + len(q_dtype + kv_dtype))
+    ref, _ = oracle_out(inp)
+    for S in (1, 3):
+        out, plan, _ = run_gpu(inp, TCI8, splits=S)
+        assert plan.kernel == TCI8
+        assert_close(out, ref, wl.kv_dtype, f"widening {kv_dtype} q {q_dtype} Hq{Hq} Hkv{Hkv} Lq{Lq} D{D} S{S}")
+
+
+@pytest.mark.parametrize("bs", [8, 64, 128])
+def test_widening_kernel_16bit_block_sizes(bs):
+    wl = W.window_sink_bf16(batch=3).replace(ctx=[2500, 333, 129], Hq=32, Hkv=4, Lq=4, bs=bs, window=0, sinks=False,
+                                             extra_pages=3)
+    inp = _inputs(wl, 250 + bs)
+    ref, _ = oracle_out(inp)
+    for S in (1, 4):
+        out, plan, _ = run_gpu(inp, TCI8, splits=S)
+        assert plan.kernel == TCI8
+        assert_close(out, ref, wl.kv_dtype, f"widening bf16 bs{bs} S{S}")
+
+
+def test_widening_kernel_bf16_tile_magnitudes():
+    """The per-tile power of two of a bf16 cache: pages whose K and V values sit anywhere from
+    2^-60 to 2^60 (tiles of very different size in one split), and pages holding elements 2^-30 of
+    their largest, all match the oracle (the conditioned bound: outputs that are small
+    differences of large terms)."""
+    wl = W.window_sink_bf16(batch=2).replace(ctx=[3000, 900], Hq=32, Hkv=4, Lq=4, window=0, sinks=False,
+                                             extra_pages=2)
+    inp = _inputs(wl, 260, poison=False)
+    exps_v = [-60, -20, -3, 0, 5, 17, 60]
+    exps_k = [-12, -4, 0, 2, 3]
+    for b in range(wl.B):
+        n = (wl.ctx[b] + wl.bs - 1) // wl.bs
+        pages = inp.block_table[b, :n].long()
+        for i, pg in enumerate(pages.tolist()):
+            inp.v_cache[pg] *= 2.0 ** exps_v[(i + b) % len(exps_v)]
+            inp.k_cache[pg] *= 2.0 ** exps_k[(3 * i + b) % len(exps_k)]
+    inp.v_cache[..., ::5] *= 2.0 ** -30
+    ref, _ = oracle_out(inp)
+    cond, _ = oracle_out(abs_value_inputs(inp))
+    for S in (1, 3):
+        out, plan, _ = run_gpu(inp, TCI8, splits=S)
+        assert plan.kernel == TCI8
+        assert_close_conditioned(out, ref, cond, wl.kv_dtype, f"widening bf16 magnitudes S{S}")
+
+
+@pytest.mark.parametrize("kv_dtype,D,Lq", [("bf16", 128, 4), ("f16", 64, 16), ("bf16", 64, 2)])
+def test_auto_takes_the_widening_kernel_for_16bit_caches(kv_dtype, D, Lq):
+    """AUTO sends 16-bit caches the 16-bit tensor-core kernel does not take to the widening
+    kernel (not the generic one), and the result matches the oracle."""
+    wl = W.window_sink_bf16(batch=3).replace(ctx=[2000, 300, 40], Hq=32, Hkv=4, Lq=Lq, D=D, q_dtype="bf16",
+                                             kv_dtype=kv_dtype, extra_pages=2)
+    inp = _inputs(wl, 270 + D + Lq)
+    ref, _ = oracle_out(inp)
+    out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_AUTO)
+    assert plan.kernel == TCI8
+    assert_close(out, ref, wl.kv_dtype, f"auto {kv_dtype} D{D} Lq{Lq}")
