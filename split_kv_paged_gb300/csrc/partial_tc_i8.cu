@@ -22,8 +22,8 @@
 //                 K and V rows (64-token tiles) into a 3-stage staging ring, with the tile's
 //                 scales (cp.async) and page mask, so three tiles of HBM reads are in flight;
 //   warps 12..15  converters: widen a staged tile to f16 in the 128-byte-swizzle layout the
-//                 MMAs read (rows = tokens, 64-element atoms): warps 12, 13 the K half once the
-//                 previous tile's QK^T is done, warps 14, 15 the V half once the previous tile's
+//                 MMAs read (rows = tokens, 64-element atoms), all four warps on the K half once
+//                 the previous tile's QK^T is done, then on the V half once the previous tile's
 //                 PV is done (one f16 stage); the tile's scales, page mask and largest V scale go
 //                 to a 4-slot meta ring;
 //   warp 1        one thread issues every QK^T: A = Q in TMEM (written once per item), B = the
@@ -33,11 +33,12 @@
 //   warps 4..11   softmax: two threads per packed row (TMEM lane), one per 32-token half of
 //                 the tile; they exchange their row maxima through shared memory, keep the same
 //                 running (maximum, P scale) and their own partial sums. Online softmax in log2
-//                 units (tiny-llm PR #11: per-split online (m, l, acc)). P times the V scale is
-//                 rounded once to f16 (2^-11 relative), with a power-of-two factor 2^C that keeps
-//                 it inside f16's range: C follows the largest V scale seen, only ever
-//                 decreases, and O is then rescaled exactly (each thread of a row its half of
-//                 the columns).
+//                 units (tiny-llm PR #11: per-split online (m, l, acc)); a row's exponent
+//                 reference moves only when a tile's maximum passes it by more than kSlack, so O
+//                 is rarely rescaled. P times the V scale is rounded once to f16 (2^-11
+//                 relative), with a power-of-two factor 2^C that keeps it inside f16's range: C
+//                 follows the largest V scale seen, only ever decreases, and O is then rescaled
+//                 exactly (each thread of a row its half of the columns).
 //
 // Every wait is bounded in time; a timeout sets TLLM_FLAG_TIMEOUT, lets every role run to its
 // end without waiting, skips the output stores, takes no further item and frees TMEM.
@@ -61,6 +62,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;   // Q: D/2 columns, S: 2 x 64, O: D
 constexpr int kEpiStride = 36;          // floats per staged output row (32 + 4: conflict-free float4 rows)
 constexpr int kSmThreads = 256;         // softmax: 8 warps, two threads per TMEM lane
+// Slack of a row's exponent reference M (log2 units): M moves only when a tile's row maximum
+// passes it by more than kSlack, so P = 2^(score - M) stays below 2^kSlack and the O rescale (a
+// TMEM round trip that waits for the previous tile's PV) is rare; the P scale 2^C leaves room.
+constexpr int kSlack = 2;
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(kThreads)
   const int brows = bs < kT ? bs : kT;                     // rows of one TMA box
   const int ppt = bs < kT ? kT >> bs_sh : 1;               // pages a tile touches
   // exchange floats of the two threads of a row: [0, 512) tile row maxima [parity][half][row],
-  // [512, 768) query maxima [half][row], [768, 1024) row sums [half][row]; [1024, 1026) the K
+  // [512, 768) query maxima [half][row], [768, 1024) row sums [half][row]; [1024, 1028) the
   // converter warps' tile maxima (bf16 K)
   float* xf = reinterpret_cast<float*>(sm + S::kOffX);
 
@@ -196,9 +201,9 @@ __global__ void __launch_bounds__(kThreads)
       mbar_init(bars.full8(s), 1 + 32 + 1);                // expect_tx + 32 lanes' scale copies + mask
       mbar_init(bars.empty8(s), 4);                        // one elected lane per converter warp
     }
-    mbar_init(bars.fullK(), 2);                            // one elected lane per K converter warp
+    mbar_init(bars.fullK(), 4);                            // one elected lane per converter warp
     mbar_init(bars.emptyK(), 1);
-    mbar_init(bars.fullV(), 2);                            // one elected lane per V converter warp
+    mbar_init(bars.fullV(), 4);
     mbar_init(bars.emptyV(), 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(bars.s_full(s), 1);
@@ -320,15 +325,14 @@ __global__ void __launch_bounds__(kThreads)
     // (an aligned barrier) converged
     __syncwarp();
   } else if (warp >= 12) {
-    // ---------------- converters: a staged tile -> f16 tile, scales and mask ----------------
-    // Warps 12, 13 widen K, warps 14, 15 widen V, each pair at its own pace: K(j + 1) waits only
-    // for the QK^T of tile j, V(j + 1) only for the PV of tile j.
+    // ---------------- converters: a staged tile -> f16 tiles, scales and mask ----------------
+    // Warps 12..15 widen each tile's K half, then its V half, all four warps on each: K(j) once
+    // the QK^T of tile j - 1 is done, V(j) once the PV of tile j - 1 is done. Widening K(j + 1)
+    // then overlaps the PV of tile j, which the V half of tile j + 1 waits for.
     const int ct = tid - 384;                              // 0..127
-    const int which = ct >> 6;                             // 0: K, 1: V
-    const int cw = ct & 63;                                // thread within the pair
     constexpr int kEpc = 16 / kEsz;                        // elements per 16-byte chunk
-    constexpr int kChunksPerRow = D / kEpc, kPer = kT * kChunksPerRow / 64;
-    float* xc = xf + 1024;                                 // the K pair's tile maxima (bf16 K)
+    constexpr int kChunksPerRow = D / kEpc, kPer = kT * kChunksPerRow / 128;
+    float* xc = xf + 1024;                                 // the converter warps' tile maxima (bf16 K)
     for (int j = 0; j < n_tiles; j++) {
       const int st = j % kStages8;
       if (!mbar_wait(bars.full8(st), (j / kStages8) & 1, abort)) set_abort_i8(abort, p.status);
@@ -342,121 +346,123 @@ __global__ void __launch_bounds__(kThreads)
         const int slot = bs < kT ? t >> bs_sh : 0;
         return ((pmask8 >> slot) & 1) && tt + t >= vlo && tt + t < t1;
       };
-      // this thread's chunks of its operand, loaded before anything is converted (their
-      // latencies overlap)
-      uint4 w[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; i++) {
-        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
-        w[i] = *reinterpret_cast<const uint4*>(src + which * S::kRaw + (t * D + d0) * kEsz);
-      }
-      // A bf16 K tile enters f16 scaled by 2^e, e from the largest |x| the split reads in it, so
-      // that this maximum lies in [2^13, 2^14): every element within 2^-27 of it converts to a
-      // normal f16 exactly (bf16 keeps 8 significant bits, f16 11); a smaller one rounds by at
-      // most 2^-38 of the maximum, below the fp32 rounding bound of the score it enters. 2^-e
-      // goes to the tile's per-token scales. An f16 tile, and a bf16 V tile, is copied as it is
-      // (e = 0).
-      int e = 0;
-      if (kKv == kKvBf16 && which == 0) {
-        float mx = 0.f;
+      for (int which = 0; which < 2; which++) {
+        // this thread's chunks of the operand, loaded before anything is converted (their
+        // latencies overlap)
+        uint4 w[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
-          const int t = (cw + 64 * i) / kChunksPerRow;
-          if (read_tok(t)) {
-            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-              mx = fmax3(mx, fabsf(__uint_as_float(ws[k] << 16)), fabsf(__uint_as_float(ws[k] & 0xffff0000u)));
-          }
+          const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+          w[i] = *reinterpret_cast<const uint4*>(src + which * S::kRaw + (t * D + d0) * kEsz);
         }
-        mx = warp_max_abs(isfinite(mx) ? mx : 0.f);
-        if (lane == 0) xc[warp - 12] = mx;
-        named_bar(2, 64);                                  // the K pair, warps 12 and 13
-        mx = fmaxf(xc[0], xc[1]);
-        named_bar(2, 64);                                  // both read before the next tile's write
-        if (mx > 0.f) e = min(125, max(-125, 14 - exponent_of(mx)));
-      }
-      // The tile's meta, into ring slot j % 4: scales (K by the K pair, V by the V pair), the
-      // page mask and the tile's largest |V scale|. The K scales leave here multiplied by the
-      // softmax scale in log2 units, so that a score reaches the softmax as one product with the
-      // query row's power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax
-      // is over: tile j's copies were issued after both pairs released tile j - 3's stage, and
-      // the V pair widened tile j - 3 only after the PV of tile j - 4, which waited for that
-      // softmax.
-      {
-        float scv;
-        if constexpr (k16) scv = __int_as_float((127 - e) << 23);    // 2^-e, the same for every token
-        else scv = reinterpret_cast<const float*>(src + 2 * S::kRaw)[ct];
-        uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
-        reinterpret_cast<float*>(meta)[ct] = ct < kT ? scv * p.scale_log2 : scv;
-        const float vm = warp_max_abs(ct >= kT && isfinite(scv) ? scv : 0.f);
-        if (ct == 0) *reinterpret_cast<uint32_t*>(meta + S::kSc) = pmask8;
-        if (lane == 0 && ct >= kT) reinterpret_cast<float*>(meta + S::kSc + 4)[(ct - kT) >> 5] = vm;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
-      }
-      // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
-      if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
-        set_abort_i8(abort, p.status);
-      const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
-      const float emul = __int_as_float((e + 127) << 23);
+        // A bf16 K tile enters f16 scaled by 2^e, e from the largest |x| the split reads in it,
+        // so that this maximum lies in [2^13, 2^14): every element within 2^-27 of it converts to
+        // a normal f16 exactly (bf16 keeps 8 significant bits, f16 11); a smaller one rounds by
+        // at most 2^-38 of the maximum, below the fp32 rounding bound of the score it enters.
+        // 2^-e goes to the tile's per-token K scales. An f16 tile, and a bf16 V tile, is copied
+        // as it is (e = 0).
+        int e = 0;
+        if (kKv == kKvBf16 && which == 0) {
+          float mx = 0.f;
 #pragma unroll
-      for (int i = 0; i < kPer; i++) {
-        const int c = cw + 64 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
-        // V rows of tokens the split does not read become zero: their bytes may be NaN (an e4m3
-        // or 16-bit code), and the PV MMA would carry 0 x NaN. (K needs no such care: the
-        // softmax selects -inf for those tokens' scores.) Int8 codes are always finite.
-        const bool ok = kKv == kKvI8 || which == 0 || read_tok(t);
-        const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-        const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
-        const uint32_t byte = (d0 & 63) * 2;
-        if constexpr (!k16) {
-          uint32_t h[8];
-          if constexpr (kKv == kKvE4m3) {
-            // two e4m3 codes -> f16x2, element 0 (the lower byte) in the low half
+          for (int i = 0; i < kPer; i++) {
+            const int t = (ct + 128 * i) / kChunksPerRow;
+            if (read_tok(t)) {
+              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-            for (int q = 0; q < 8; q++) h[q] = ok ? e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1)))) : 0u;
-          } else {
-            // int8 -> f16 exactly: the byte, sign bit flipped, placed under the f16 exponent of
-            // 1024 reads 1024 + (x + 128); subtracting 1152 leaves x
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-              const uint32_t x = __byte_perm(ws[q >> 1] ^ 0x80808080u, 0x64646464u, (q & 1) ? 0x5342u : 0x5140u);
-              const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
-              h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+              for (int k = 0; k < 4; k++)
+                mx = fmax3(mx, fabsf(__uint_as_float(ws[k] << 16)), fabsf(__uint_as_float(ws[k] & 0xffff0000u)));
             }
           }
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
-                       "r"(h[2]), "r"(h[3]));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
-                       "r"(h[5]), "r"(h[6]), "r"(h[7]));
-        } else {
-          uint32_t h[4];
+          mx = warp_max_abs(isfinite(mx) ? mx : 0.f);
+          if (lane == 0) xc[warp - 12] = mx;
+          named_bar(2, 128);                               // the four converter warps
+          mx = fmaxf(fmaxf(xc[0], xc[1]), fmaxf(xc[2], xc[3]));
+          named_bar(2, 128);                               // all read before the next tile's write
+          if (mx > 0.f) e = min(125, max(-125, 14 - exponent_of(mx)));
+        }
+        if (which == 0) {
+          // The tile's meta, into ring slot j % 4: scales (thread ct: the K scale of token ct
+          // for ct < 64, else the V scale of token ct - 64), the page mask and the tile's
+          // largest |V scale|. The K scales leave here multiplied by the softmax scale in log2
+          // units, so that a score reaches the softmax as one product with the query row's
+          // power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax is
+          // over: tile j's copies were issued after the converters released tile j - 3's stage,
+          // which they did after widening V(j - 3), after the PV of tile j - 4, which waited for
+          // that softmax.
+          float scv;
+          if constexpr (k16) scv = ct < kT ? __int_as_float((127 - e) << 23) : 1.f;   // 2^-e for K
+          else scv = reinterpret_cast<const float*>(src + 2 * S::kRaw)[ct];
+          uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
+          reinterpret_cast<float*>(meta)[ct] = ct < kT ? scv * p.scale_log2 : scv;
+          const float vm = warp_max_abs(ct >= kT && isfinite(scv) ? scv : 0.f);
+          if (ct == 0) *reinterpret_cast<uint32_t*>(meta + S::kSc) = pmask8;
+          if (lane == 0 && ct >= kT) reinterpret_cast<float*>(meta + S::kSc + 4)[(ct - kT) >> 5] = vm;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
+        }
+        // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
+        if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
+          set_abort_i8(abort, p.status);
+        const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
+        const float emul = __int_as_float((e + 127) << 23);
 #pragma unroll
-          for (int q = 0; q < 4; q++) {
-            if (kKv == kKvBf16 && which == 0) {
-              const __half2 v2 = __floats2half2_rn(__uint_as_float(ws[q] << 16) * emul,
-                                                   __uint_as_float(ws[q] & 0xffff0000u) * emul);
-              h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+        for (int i = 0; i < kPer; i++) {
+          const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+          // V rows of tokens the split does not read become zero: their bytes may be NaN (an
+          // e4m3 or 16-bit code), and the PV MMA would carry 0 x NaN. (K needs no such care:
+          // the softmax selects -inf for those tokens' scores.) Int8 codes are always finite.
+          const bool ok = kKv == kKvI8 || which == 0 || read_tok(t);
+          const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+          const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
+          const uint32_t byte = (d0 & 63) * 2;
+          if constexpr (!k16) {
+            uint32_t h[8];
+            if constexpr (kKv == kKvE4m3) {
+              // two e4m3 codes -> f16x2, element 0 (the lower byte) in the low half
+#pragma unroll
+              for (int q = 0; q < 8; q++) h[q] = ok ? e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1)))) : 0u;
             } else {
-              h[q] = ok ? ws[q] : 0u;
+              // int8 -> f16 exactly: the byte, sign bit flipped, placed under the f16 exponent
+              // of 1024 reads 1024 + (x + 128); subtracting 1152 leaves x
+#pragma unroll
+              for (int q = 0; q < 8; q++) {
+                const uint32_t x = __byte_perm(ws[q >> 1] ^ 0x80808080u, 0x64646464u, (q & 1) ? 0x5342u : 0x5140u);
+                const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+                h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+              }
             }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
+                         "r"(h[2]), "r"(h[3]));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte + 16)), "r"(h[4]),
+                         "r"(h[5]), "r"(h[6]), "r"(h[7]));
+          } else {
+            uint32_t h[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              if (kKv == kKvBf16 && which == 0) {
+                const __half2 v2 = __floats2half2_rn(__uint_as_float(ws[q] << 16) * emul,
+                                                     __uint_as_float(ws[q] & 0xffff0000u) * emul);
+                h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+              } else {
+                h[q] = ok ? ws[q] : 0u;
+              }
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
+                         "r"(h[2]), "r"(h[3]));
           }
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
-                       "r"(h[2]), "r"(h[3]));
         }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(which == 0 ? bars.fullK() : bars.fullV());
       }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(which == 0 ? bars.fullK() : bars.fullV());
-        mbar_arrive(bars.empty8(st));
-      }
+      if (lane == 0) mbar_arrive(bars.empty8(st));
     }
-    // the release of the f16 stage by the last tile's MMA (an asynchronous tcgen05.commit
-    // arrival) must have landed before the next item re-initialises the barriers
-    if (!mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (n_tiles - 1) & 1, abort))
-      set_abort_i8(abort, p.status);
+    // the releases of the f16 stage by the last tile's MMAs (asynchronous tcgen05.commit
+    // arrivals) must have landed before the next item re-initialises the barriers
+    if (!mbar_wait(bars.emptyK(), (n_tiles - 1) & 1, abort)) set_abort_i8(abort, p.status);
+    if (!mbar_wait(bars.emptyV(), (n_tiles - 1) & 1, abort)) set_abort_i8(abort, p.status);
   } else if (warp >= 4) {
     // ---------------- softmax: two threads per packed row r (TMEM lane), one per token half ----------------
     const int hh = (warp - 4) >> 2;                        // token half (0: tokens 0..31, 1: 32..63)
@@ -607,19 +613,20 @@ __global__ void __launch_bounds__(kThreads)
       xm[128 * hh + r] = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       named_bar(1, kSmThreads);
       const float mx = fmaxf(xm[r], xm[128 + r]);
-      // P scale exponent C: vmax * 2^C < 2^14; it only ever decreases (then O is rescaled)
+      // P scale exponent C: vmax * 2^C < 2^(14 - kSlack); it only ever decreases (then O is
+      // rescaled)
       if (vmax > 0.f) {
         int ex;
         frexpf(vmax, &ex);
-        C = min(C, min(60, max(-60, 14 - ex)));
+        C = min(C, min(60, max(-60, 14 - kSlack - ex)));
       } else if (C == (1 << 20)) {
         C = 0;
       }
-      // p' = 2^(u qscale + e0) with e0 = C - M (rounded): the row's largest term is 2^C. O and l
-      // are kept in units of 2^-e0 for the e0 actually used, so its rounding cancels in O / l
-      // and in the LSE (log2 l - e0), and a change of e0 rescales both by 2^(e0 - e0_prev).
-      // Both threads of a row hold the same M, C and e0.
-      const float M_new = fmaxf(M, mx * qscale);
+      // p' = 2^(u qscale + e0) with e0 = C - M (rounded): the row's largest term is at most
+      // 2^(C + kSlack). O and l are kept in units of 2^-e0 for the e0 actually used, so its
+      // rounding cancels in O / l and in the LSE (log2 l - e0), and a change of e0 rescales both
+      // by 2^(e0 - e0_prev). Both threads of a row hold the same M, C and e0.
+      const float M_new = mx * qscale > M + (float)kSlack ? mx * qscale : M;
       const float e0 = M_new == -INFINITY ? 0.f : (float)C - M_new;
       const float factor = M == -INFINITY ? (M_new == -INFINITY ? 1.f : 0.f) : ex2f(e0 - e0_run);
       e0_run = e0;
