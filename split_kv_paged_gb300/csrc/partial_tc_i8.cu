@@ -391,9 +391,12 @@ __global__ void __launch_bounds__(kThreads)
           // over: tile j's copies were issued after the converters released tile j - 3's stage,
           // which they did after widening V(j - 3), after the PV of tile j - 4, which waited for
           // that softmax.
+          // A token the split does not read gets zero scales (its staged scale may be stale or
+          // NaN), so that the softmax's P x V-scale product is 0 there without a select.
           float scv;
           if constexpr (k16) scv = ct < kT ? __int_as_float((127 - e) << 23) : 1.f;   // 2^-e for K
           else scv = reinterpret_cast<const float*>(src + 2 * S::kRaw)[ct];
+          if (!read_tok(ct & (kT - 1))) scv = 0.f;
           uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
           reinterpret_cast<float*>(meta)[ct] = ct < kT ? scv * p.scale_log2 : scv;
           const float vm = warp_max_abs(ct >= kT && isfinite(scv) ? scv : 0.f);
@@ -643,8 +646,9 @@ __global__ void __launch_bounds__(kThreads)
         // e0 = 0, every u = -inf)
         const float2 p01 = make_float2(ex2f(x01.x), ex2f(x01.y)), p23 = make_float2(ex2f(x23.x), ex2f(x23.y));
         ls = fadd2(ls, fadd2(p01, p23));
-        const float w0 = p01.x != 0.f ? p01.x * v.x : 0.f, w1 = p01.y != 0.f ? p01.y * v.y : 0.f;
-        const float w2 = p23.x != 0.f ? p23.x * v.z : 0.f, w3 = p23.y != 0.f ? p23.y * v.w : 0.f;
+        // (the V scale of a token the split does not read is 0, and its p is 0 too)
+        const float2 w01 = fmul2(p01, make_float2(v.x, v.y)), w23 = fmul2(p23, make_float2(v.z, v.w));
+        const float w0 = w01.x, w1 = w01.y, w2 = w23.x, w3 = w23.y;
         if constexpr (kPParts == 2) {
           const __nv_bfloat162 h01 = __floats2bfloat162_rn(w0, w1), h23 = __floats2bfloat162_rn(w2, w3);
           const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
