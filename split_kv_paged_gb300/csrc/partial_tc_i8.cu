@@ -65,7 +65,7 @@ constexpr int kSmThreads = 256;         // softmax: 8 warps, two threads per TME
 // Slack of a row's exponent reference M (log2 units): M moves only when a tile's row maximum
 // passes it by more than kSlack, so P = 2^(score - M) stays below 2^kSlack and the O rescale (a
 // TMEM round trip that waits for the previous tile's PV) is rare; the P scale 2^C leaves room.
-constexpr int kSlack = 2;
+constexpr int kSlack = 4;
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
