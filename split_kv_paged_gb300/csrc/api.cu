@@ -62,7 +62,7 @@ KernelTraits traits(int kernel, const tllm_decode_attn_desc& d, int rows) {
 
   switch (kernel) {
     case TLLM_KERNEL_TC_FP8: return KernelTraits{128, 1, 1, 1024, false, 512, true};
-    case TLLM_KERNEL_SIMT: return KernelTraits{simt_tile(d.head_dim), 2, 1, 256};
+    case TLLM_KERNEL_SIMT: return KernelTraits{simt_tile(d.head_dim), 2, (rows + 7) / 8, 256};
     case TLLM_KERNEL_TC_I8: return KernelTraits{64, 1, 1, 512, false, 128, true};
     case TLLM_KERNEL_TC_B16: return KernelTraits{128, 1, 1, 256, true, 700};
     default: return KernelTraits{32, 2, (rows + 15) / 16, 64};
@@ -294,8 +294,9 @@ tllm_status tllm_decode_attn_plan(const tllm_decode_attn_desc* desc, int32_t bat
                               align256(units * (size_t)d.head_dim * rec_bytes);
   // Fused combine, when asked for: the CTA that writes a request's last split record merges
   // them all, so no combine kernel is launched. Only where that merge is small next to the
-  // call: the CUDA-core few-row kernel with at most 128 KB of records per request.
-  out_plan->fused_combine = d.combine_mode == TLLM_COMBINE_FUSED && kernel == TLLM_KERNEL_SIMT && S > 1 &&
+  // call: the CUDA-core few-row kernel (one row block: at most 8 rows) with at most 128 KB of
+  // records per request.
+  out_plan->fused_combine = d.combine_mode == TLLM_COMBINE_FUSED && kernel == TLLM_KERNEL_SIMT && S > 1 && rows <= 8 &&
                             (size_t)S * rows * d.head_dim * rec_bytes <= ((size_t)128 << 10);
   return TLLM_OK;
 }

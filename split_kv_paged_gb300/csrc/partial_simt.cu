@@ -3,8 +3,11 @@
 // plain GQA (R = G) is this shape; with so few rows per KV head a tensor-core tile would be
 // mostly padding, and the kernel is bound by the HBM stream alone.
 //
-// One CTA = one (request, kv head, split), 256 threads; each KV byte of the split is read
-// once (GQA packing: "split packed-Q8 verifier KV scans", hipfire PR #760, Summary).
+// One CTA = one (request, kv head, split, block of 8 packed rows), 256 threads; with at most 8
+// rows there is one row block and each KV byte of the split is read once (GQA packing: "split
+// packed-Q8 verifier KV scans", hipfire PR #760, Summary). More rows (the shapes no tensor-core
+// kernel takes: 16-bit caches at head_dim 256) run as several row blocks, each reading the
+// split's KV (the later reads mostly from L2).
 //   Load:    all threads copy tile j + kStages - 1 (K rows, V rows and, for quantised KV, the
 //            per-token scales) with 16-byte cp.async into a kStages-deep shared-memory ring;
 //            tokens the split does not read, or on an invalid page, are zero-filled. Page
@@ -186,9 +189,10 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.x, b = u / p.Hkv, g = u % p.Hkv, split = blockIdx.y;
+  const int r0 = blockIdx.z * RM;                          // first packed row of this CTA's block
   const int raw_ctx = p.context_lens[b];
   const int ctx = clamp_ctx(raw_ctx, p.max_ctx);
-  if (raw_ctx != ctx && tid == 0 && split == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
+  if (raw_ctx != ctx && tid == 0 && split == 0 && r0 == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
   const Span sp = request_span(ctx, p.Lq, p.window, p.num_splits, p.min_chunk, p.align);
   if (split >= sp.nsplit) return;
   const int t0 = sp.base + split * sp.chunk;
@@ -211,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
     VecF32<S::kDpl> qv[RM];                                // all rows' loads in flight together
 #pragma unroll
     for (int r = 0; r < RM; r++) {
-      const bool real = r < p.R;
-      const int qi = real ? r / p.G : 0, h = g * p.G + (real ? r % p.G : 0);
+      const bool real = r0 + r < p.R;
+      const int qi = real ? (r0 + r) / p.G : 0, h = g * p.G + (real ? (r0 + r) % p.G : 0);
       qv[r].load(p.q, p.q_dtype, ((int64_t)(b * p.Lq + qi) * p.Hq + h) * D + li * S::kDpl, real);
     }
 #pragma unroll
@@ -225,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
   // after the reduction each lane owns the softmax state of one row: rho
   constexpr int kLpr = S::kLpt / RM;                       // lanes per row
   const int rho = li / kLpr;
-  const int pos_rho = rho < p.R ? ctx - p.Lq + rho / p.G : -1;   // its position (-1: no keys)
+  const int pos_rho = r0 + rho < p.R ? ctx - p.Lq + (r0 + rho) / p.G : -1;   // its position (-1: no keys)
   const int gbase = lane - li;                             // first lane of the group
 
   const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
@@ -401,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
   }
   __syncthreads();
   for (int idx = tid; idx < RM * D; idx += kThreads) {
-    const int r = idx / D, d = idx % D;
-    if (r >= p.R) continue;
+    const int r = idx / D, d = idx % D, rg = r0 + r;     // row in the block, packed row
+    if (rg >= p.R) continue;
     float M = -INFINITY;
     for (int gi = 0; gi < S::kGroups; gi++) M = fmaxf(M, ml[(gi * RM + r) * 2]);
     float L = 0.f, O = 0.f;
@@ -414,18 +418,19 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
         O = fmaf(w, mo[(gi * RM + r) * D + d], O);
       }
     }
-    const int qi = r / p.G, h = g * p.G + r % p.G;
+    const int qi = rg / p.G, h = g * p.G + rg % p.G;
     if (finalize) {
       float den = L;
       if (p.sinks && M != -INFINITY) den += ex2s(p.sinks[h] * kLog2e - M);
       store_f32(p.out, p.out_dtype, ((int64_t)(b * p.Lq + qi) * p.Hq + h) * D + d, L > 0.f ? O / den : 0.f);
     } else {
-      store_rec(p, ((int64_t)u_split * p.R + r) * D + d, L > 0.f ? O / L : 0.f);
-      if (d == 0) p.ws_lse[(int64_t)u_split * p.R + r] = L > 0.f ? M + log2f(L) : -INFINITY;
+      store_rec(p, ((int64_t)u_split * p.R + rg) * D + d, L > 0.f ? O / L : 0.f);
+      if (d == 0) p.ws_lse[(int64_t)u_split * p.R + rg] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
   }
   // fused combine: the CTA that completes the request's records merges them into the output
-  if (!finalize && p.fused) {
+  // (planned only with one row block)
+  if (!finalize && p.fused && gridDim.z == 1) {
     __shared__ int last_arrival;
     __syncthreads();                                       // the merge area below is free again
     fused_combine_arrive(p, u, b, g, sp.nsplit, &last_arrival, reinterpret_cast<float*>(smem));
@@ -470,8 +475,7 @@ bool simt_supports(const tllm_decode_attn_desc& d, int rows) {
   const bool kv_ok = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16 || d.kv_dtype == TLLM_FP8_E4M3 ||
                      d.kv_dtype == TLLM_INT8;
   return kv_ok && d.v_layout == TLLM_V_TOKEN_MAJOR && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) &&
-         rows >= 1 && rows <= 8 &&
-         (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128);
+         rows >= 1 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128);
 }
 
 int simt_tile(int) { return kTile; }
@@ -482,8 +486,9 @@ bool simt_pointers_ok(const Params& p) {
 }
 
 cudaError_t launch_partial_simt(const Params& p, cudaStream_t stream) {
-  dim3 grid(p.B * p.Hkv, p.num_splits);
-  return p.R <= 4 ? launch_kt<4>(p, grid, stream) : launch_kt<8>(p, grid, stream);
+  const int rm = p.R <= 4 ? 4 : 8;                          // rows per CTA
+  dim3 grid(p.B * p.Hkv, p.num_splits, (p.R + rm - 1) / rm);
+  return rm == 4 ? launch_kt<4>(p, grid, stream) : launch_kt<8>(p, grid, stream);
 }
 
 }  // namespace tllm

@@ -904,3 +904,35 @@ def test_auto_takes_the_widening_kernel_for_16bit_caches(kv_dtype, D, Lq):
     out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_AUTO)
     assert plan.kernel == TCI8
     assert_close(out, ref, wl.kv_dtype, f"auto {kv_dtype} D{D} Lq{Lq}")
+
+
+# --- the CUDA-core kernel in row blocks (more than 8 packed rows) -------------------------------
+
+@pytest.mark.parametrize("q_dtype,kv_dtype", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f16")])
+@pytest.mark.parametrize("Hq,Hkv,Lq", [(32, 4, 2), (16, 1, 4), (12, 4, 3)])
+def test_simt_row_blocks_head_dim_256_16bit(Hq, Hkv, Lq, q_dtype, kv_dtype):
+    """16-bit caches at head_dim 256 with 9..64 packed rows (no tensor-core kernel takes them):
+    AUTO runs the CUDA-core kernel in blocks of 8 rows, the last one ragged, with a window,
+    sinks, ragged lengths and poisoned tails."""
+    wl = W.window_sink_bf16(batch=4).replace(ctx=[2600, 700, 65, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=256, q_dtype=q_dtype,
+                                             kv_dtype=kv_dtype, window=900, bs=16, extra_pages=4)
+    inp = _inputs(wl, 280 + Hq + Lq + len(q_dtype + kv_dtype))
+    ref, _ = oracle_out(inp)
+    for S in (1, 3):
+        out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_AUTO, splits=S)
+        assert plan.kernel == B.TLLM_KERNEL_SIMT
+        assert_close(out, ref, wl.kv_dtype, f"simt rows {Hq // Hkv * Lq} {kv_dtype} q {q_dtype} S{S}")
+
+
+@pytest.mark.parametrize("kv_dtype,D,Hq,Hkv,Lq", [("f16", 128, 24, 1, 1), ("i8", 64, 12, 2, 2), ("e4m3", 128, 20, 1, 2)])
+def test_simt_row_blocks_pinned(kv_dtype, D, Hq, Hkv, Lq):
+    """The CUDA-core kernel pinned on shapes with more than 8 rows (3 to 5 row blocks) for the
+    other cache types and head_dims."""
+    wl = W.verify16_int8().replace(ctx=[1900, 300, 40], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, kv_dtype=kv_dtype, q_dtype="bf16",
+                                   extra_pages=2)
+    inp = _inputs(wl, 290 + D + Hq)
+    ref, _ = oracle_out(inp)
+    for S in (1, 4):
+        out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_SIMT, splits=S)
+        assert plan.kernel == B.TLLM_KERNEL_SIMT
+        assert_close(out, ref, wl.kv_dtype, f"simt pinned {kv_dtype} D{D} rows {Hq // Hkv * Lq} S{S}")
