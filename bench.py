@@ -396,6 +396,48 @@ def other_config(name, wl, seed, dev, stream, peak, steps, warmup, splits=0):
     return name, rec
 
 
+def option_config(m, record, v_dim_major, steps, warmup, peak):
+    """The headline workload with one descriptor option (16-bit split records, or the V cache
+    in the transposed, dimension-major layout): the same inputs (V copied into that layout),
+    its own plan and workspace, timed the same way as the headline (graph replays)."""
+    B, wl, inp, dev, stream = m.B, m.wl, m.inp, m.dev, m.stream
+    rec = {"f32": B.TLLM_RECORD_F32, "bf16": B.TLLM_RECORD_BF16, "f16": B.TLLM_RECORD_F16}[record]
+    vl = B.TLLM_V_DIM_MAJOR if v_dim_major else B.TLLM_V_TOKEN_MAJOR
+    desc = B.desc_for(wl, B.TLLM_KERNEL_AUTO, num_pages=inp.num_pages, v_layout=vl, record_type=rec)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, num_sms=n_sm)
+    ws = B.Workspace(plan, device=dev)
+    out = torch.empty_like(m.out)
+    v = inp.v_cache.transpose(-1, -2).contiguous() if v_dim_major else inp.v_cache
+    call = (inp.q, inp.k_cache, v, inp.block_table, inp.context_lens, wl.Lq, inp.kv_scales, inp.sinks, wl.window,
+            plan.num_splits, ws, out)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            B.tllm_decode_attn_splitkv(*call, stream=stream)
+        torch.cuda.synchronize(dev)
+        graphs = []
+        for fn in (B.tllm_decode_attn_splitkv, B.tllm_decode_attn_partial):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(*call, stream=stream)
+            for _ in range(max(1, warmup)):
+                g.replay()
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+    # the default descriptor's call and partial timed right before, under the same clocks
+    base_call_ms, _ = m.timed(m.g_call, steps)
+    base_part_ms, _ = m.timed(m.g_part, steps)
+    call_ms, call_med = m.timed(graphs[0], steps)
+    part_ms, _ = m.timed(graphs[1], steps)
+    del graphs, v, ws, out
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "record": record, "v_layout": "dim_major" if v_dim_major else "token_major",
+            "kernel": int(plan.kernel), "num_splits": int(plan.num_splits), "us_per_call": call_ms * 1e3,
+            "us_per_call_median_of_3_runs": call_med * 1e3, "partial_us": part_ms * 1e3,
+            "partial_frac": m.nbytes / (part_ms * 1e-3) / 1e9 / peak, "steps": steps,
+            "default_us_per_call": base_call_ms * 1e3, "default_partial_us": base_part_ms * 1e3}
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -470,6 +512,13 @@ def main():
                "seconds": secs}
 
     peak, peak_src = peak_hbm()
+    # the headline workload with each layout / record option of the descriptor (rank 0 of a
+    # single-rank default run)
+    options = {}
+    if rank == 0 and world == 1 and not args.no_other_configs and args.workload == "mtp4_fp8_long" \
+            and args.batch == 0 and args.ctx == 0 and args.bs == 0 and args.record == "f32" and args.kernel == "auto":
+        for name, record, vdm in (("record_bf16", "bf16", False), ("v_dim_major", "f32", True)):
+            options[name] = option_config(m, record, vdm, args.steps, max(3, min(args.warmup, 5)), peak)
     # the other measured workloads, each timed the same way (graph replays of one call), on
     # rank 0 of a single-rank run by default
     others = {}
@@ -507,6 +556,8 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (2 if S > 1 else 1),
     }
+    if options:
+        line["options"] = options
     if others:
         line["other_configs"] = others
     if cpu is not None:
