@@ -11,16 +11,17 @@
 // power of two chosen from its largest value, which then stands as the tile's per-token scale;
 // a bf16 V tile stays bf16, and the PV contraction runs in bf16 with P sent as a high part
 // plus the bf16 rounding of its remainder (about 16 significant bits of P), so V keeps bf16's
-// whole range. A bf16 Q row enters as f16 after a power-of-two scale
-// that is undone on the scores.
+// whole range. A bf16 Q row enters as f16 after a power-of-two scale that is undone on the
+// scores.
 //
 // Persistent CTAs, one per SM, take the real (request, kv head, split) items of a work list
 // built on the device from the lengths, in turn (item k to CTA k mod grid); per item each KV
 // page of the split is read from HBM once (GQA packing: "split packed-Q8 verifier KV scans",
 // hipfire PR #760, Summary). Roles (512 threads):
-//   warp 0        producer: walks the block table one tile ahead and TMA-loads each page's int8
-//                 K and V rows (64-token tiles) into a 3-stage staging ring, with the tile's
-//                 scales (cp.async) and page mask, so three tiles of HBM reads are in flight;
+//   warp 0        producer: walks the block table one tile ahead and TMA-loads each page's K
+//                 and V rows as stored (64-token tiles) into a 3-stage staging ring, with the
+//                 tile's scales (cp.async, quantised caches) and page mask, so three tiles of
+//                 HBM reads are in flight;
 //   warps 12..15  converters: widen a staged tile to f16 in the 128-byte-swizzle layout the
 //                 MMAs read (rows = tokens, 64-element atoms), all four warps on the K half once
 //                 the previous tile's QK^T is done, then on the V half once the previous tile's
@@ -36,9 +37,10 @@
 //                 units (tiny-llm PR #11: per-split online (m, l, acc)); a row's exponent
 //                 reference moves only when a tile's maximum passes it by more than kSlack, so O
 //                 is rarely rescaled. P times the V scale is rounded once to f16 (2^-11
-//                 relative), with a power-of-two factor 2^C that keeps it inside f16's range: C
-//                 follows the largest V scale seen, only ever decreases, and O is then rescaled
-//                 exactly (each thread of a row its half of the columns).
+//                 relative; bf16 V: the high and low bf16 parts), with a power-of-two factor
+//                 2^C that keeps it inside the 16-bit range: C follows the largest V scale
+//                 seen, only ever decreases, and O is then rescaled exactly (each thread of a
+//                 row its half of the columns).
 //
 // Every wait is bounded in time; a timeout sets TLLM_FLAG_TIMEOUT, lets every role run to its
 // end without waiting, skips the output stores, takes no further item and frees TMEM.
