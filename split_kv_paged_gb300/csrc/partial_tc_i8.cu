@@ -18,17 +18,18 @@
 // built on the device from the lengths, in turn (item k to CTA k mod grid); per item each KV
 // page of the split is read from HBM once (GQA packing: "split packed-Q8 verifier KV scans",
 // hipfire PR #760, Summary). Roles (512 threads):
-//   warp 0        producer: walks the block table one tile ahead and TMA-loads each page's K
-//                 and V rows as stored (64-token tiles) into a 3-stage staging ring, with the
-//                 tile's scales (cp.async, quantised caches) and page mask, so three tiles of
-//                 HBM reads are in flight;
-//   warps 12..15  converters: widen a staged tile to f16 in the 128-byte-swizzle layout the
-//                 MMAs read (rows = tokens, 64-element atoms), all four warps on the K half once
-//                 the previous tile's QK^T is done, then on the V half once the previous tile's
-//                 PV is done (one f16 stage); the tile's scales, page mask and largest V scale go
-//                 to a 4-slot meta ring;
+//   warp 0, 2     producers: walk the block table one tile ahead and TMA-load each page's K
+//                 rows (warp 0) and V rows (warp 2), as stored, in 64-token tiles into staging
+//                 rings of their own (K: 2 stages, V: 3), with the tile's scales (cp.async,
+//                 quantised caches) and page mask;
+//   warps 12..15  converters: widen staged tiles to f16 in the 128-byte-swizzle layout the
+//                 MMAs read (rows = tokens, 64-element atoms), all four warps on each, in the
+//                 order K(0), K(1), V(0), K(2), V(1), ...: K(j) into f16 K buffer j % 2 once the
+//                 QK^T of tile j - 2 is done, V(j) into the f16 V buffer once the PV of tile
+//                 j - 1 is done; the tile's scales, page mask and largest V scale go to a
+//                 4-slot meta ring with K(j);
 //   warp 1        one thread issues every QK^T: A = Q in TMEM (written once per item), B = the
-//                 f16 K tile (K-major), D = S in TMEM (two 64-column buffers);
+//                 f16 K buffer (K-major), D = S in TMEM (two 64-column buffers);
 //   warp 3        one thread issues every PV: A = P in shared memory (K-major, two buffers),
 //                 B = the f16 V tile (MN-major, atoms 64 tokens x 128 B apart), D = O in TMEM;
 //   warps 4..11   softmax: two threads per packed row (TMEM lane), one per 32-token half of
@@ -58,7 +59,6 @@ using namespace ptx;
 
 constexpr int kT = 64;                 // tokens per tile
 constexpr int kThreads = 512;
-constexpr int kStages8 = 3;            // int8 staging ring depth
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;   // Q: D/2 columns, S: 2 x 64, O: D
@@ -78,12 +78,16 @@ constexpr int kKvI8 = 0, kKvE4m3 = 1, kKvF16 = 2, kKvBf16 = 3;
 template <int D, int kEsz, int kPParts>
 struct Lay {
   static constexpr uint32_t kAtom = kT * 128;                 // bytes of one atom column of a tile
-  static constexpr uint32_t kSc = 2 * kT * 4;                 // K scales | V scales
+  static constexpr uint32_t kScT = kT * 4;                    // one operand's per-token scales
+  static constexpr uint32_t kSc = 2 * kScT;                   // K scales | V scales
   static constexpr uint32_t kMeta = kSc + 16;                 // scales | page mask | largest V scale x2
   static constexpr uint32_t kRaw = kT * D * kEsz;             // one staged operand tile (K or V) as stored
-  static constexpr uint32_t kStage8 = align1k(2 * kRaw + kSc + 16);    // K | V | scales | mask, as stored
+  static constexpr uint32_t kStage = align1k(kRaw + kScT + 16);        // rows | scales | page mask, as stored
+  static constexpr int kStK = 2, kStV = 3;                    // staging ring depths: K, V
   static constexpr uint32_t kHalf16 = kT * D * 2;                      // one f16 tile (K or V)
-  static constexpr uint32_t kOff8 = 0, kOff16 = kStages8 * kStage8, kOffP = kOff16 + 2 * kHalf16;
+  static constexpr uint32_t kOff8 = 0;                        // the staging rings: K, then V
+  static constexpr uint32_t kOffK8 = 0, kOffV8 = kStK * kStage, kOff16 = kOffV8 + kStV * kStage;
+  static constexpr uint32_t kOffP = kOff16 + 3 * kHalf16;     // f16 stage: K buffer 0 | K buffer 1 | V
   static constexpr uint32_t kPPart = 128 * 128;               // P: 128 rows x 64 tokens, 16-bit
   static constexpr uint32_t kPBuf = kPPart * kPParts;         // (bf16 V: high part | low part)
   static constexpr uint32_t kOffMeta = kOffP + 2 * kPBuf;     // meta ring: 4 tiles
@@ -93,29 +97,33 @@ struct Lay {
   static constexpr uint32_t kOffList = kOffMisc + 64;         // work list + its scan scratch
   static constexpr uint32_t kSmem = kOffList + kListWords * 4 + 1024;   // + alignment slack
   static_assert(kSmem <= 232448, "shared memory");
-  static_assert(kOff16 % 1024 == 0 && kOffP % 1024 == 0 && kOffMeta % 16 == 0 && kOffBar % 8 == 0, "alignment");
+  static_assert(kStage % 1024 == 0 && kOff16 % 1024 == 0 && kOffP % 1024 == 0 && kOffMeta % 16 == 0 &&
+                    kOffBar % 8 == 0, "alignment");
   static_assert(8 * 32 * kEpiStride * 4 <= kOffP, "output staging fits in the staging ring and f16 stage");
 };
 
-// mbarriers (8 bytes each), named by their shared-memory address. The one f16 stage has a K
-// half and a V half with their own barriers: K is free again once its QK^T is done, V once its
-// PV is done, so the converters widen K(j+1) while tile j's PV is still pending.
+// mbarriers (8 bytes each), named by their shared-memory address. K and V are staged in rings
+// of their own, so a K stage is free again as soon as its K is widened while the V stage waits
+// for its V. The f16 stage has two K buffers and one V buffer: K(j) may be widened once the
+// QK^T of tile j - 2 is done, V(j) once the PV of tile j - 1 is done.
 struct BarsI8 {
   uint32_t base;
   __device__ uint32_t at(uint32_t i) const { return base + 8u * i; }
-  __device__ uint32_t full8(int s) const { return at(0 + s); }     // staged int8 tile landed
-  __device__ uint32_t empty8(int s) const { return at(3 + s); }    // converters done with it
-  __device__ uint32_t fullK() const { return at(6); }              // f16 K written
-  __device__ uint32_t emptyK() const { return at(7); }             // its QK^T is done
-  __device__ uint32_t fullV() const { return at(8); }              // f16 V written
-  __device__ uint32_t emptyV() const { return at(9); }             // its PV is done
-  __device__ uint32_t s_full(int s) const { return at(10 + s); }   // QK^T into S buffer s done
-  __device__ uint32_t s_free(int s) const { return at(12 + s); }   // S buffer s read
-  __device__ uint32_t p_full(int s) const { return at(14 + s); }   // P buffer s written (O rescaled)
-  __device__ uint32_t pv_done(int s) const { return at(16 + s); }  // PV from P buffer s done
-  __device__ uint32_t q_full() const { return at(18); }            // Q in TMEM
-  __device__ uint32_t mma_fin() const { return at(19); }           // final commits of both issuers
-  __device__ uint32_t meta_full(int s) const { return at(20 + s); }  // meta ring slot s written
+  __device__ uint32_t fullK8(int s) const { return at(0 + s); }    // staged K tile landed
+  __device__ uint32_t emptyK8(int s) const { return at(2 + s); }   // converters done with it
+  __device__ uint32_t fullV8(int s) const { return at(4 + s); }    // staged V tile landed
+  __device__ uint32_t emptyV8(int s) const { return at(7 + s); }   // converters done with it
+  __device__ uint32_t fullK16(int b) const { return at(10 + b); }  // f16 K buffer b written
+  __device__ uint32_t emptyK16(int b) const { return at(12 + b); } // its QK^T is done
+  __device__ uint32_t fullV16() const { return at(14); }           // f16 V written
+  __device__ uint32_t emptyV16() const { return at(15); }          // its PV is done
+  __device__ uint32_t s_full(int s) const { return at(16 + s); }   // QK^T into S buffer s done
+  __device__ uint32_t s_free(int s) const { return at(18 + s); }   // S buffer s read
+  __device__ uint32_t p_full(int s) const { return at(20 + s); }   // P buffer s written (O rescaled)
+  __device__ uint32_t pv_done(int s) const { return at(22 + s); }  // PV from P buffer s done
+  __device__ uint32_t q_full() const { return at(24); }            // Q in TMEM
+  __device__ uint32_t mma_fin() const { return at(25); }           // final commits of both issuers
+  __device__ uint32_t meta_full(int s) const { return at(26 + s); }  // meta ring slot s written
 };
 
 __device__ __forceinline__ void set_abort_i8(uint32_t abort, uint32_t* status) {
@@ -199,14 +207,20 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   if (tid == 0) {
-    for (int s = 0; s < kStages8; s++) {
-      mbar_init(bars.full8(s), 1 + 32 + 1);                // expect_tx + 32 lanes' scale copies + mask
-      mbar_init(bars.empty8(s), 4);                        // one elected lane per converter warp
+    for (int s = 0; s < S::kStK; s++) {
+      mbar_init(bars.fullK8(s), 1 + 32 + 1);               // expect_tx + 32 lanes' scale copies + mask
+      mbar_init(bars.emptyK8(s), 4);                       // one elected lane per converter warp
     }
-    mbar_init(bars.fullK(), 4);                            // one elected lane per converter warp
-    mbar_init(bars.emptyK(), 1);
-    mbar_init(bars.fullV(), 4);
-    mbar_init(bars.emptyV(), 1);
+    for (int s = 0; s < S::kStV; s++) {
+      mbar_init(bars.fullV8(s), 1 + 32 + 1);
+      mbar_init(bars.emptyV8(s), 4);
+    }
+    for (int k = 0; k < 2; k++) {
+      mbar_init(bars.fullK16(k), 4);                       // one elected lane per converter warp
+      mbar_init(bars.emptyK16(k), 1);
+    }
+    mbar_init(bars.fullV16(), 4);
+    mbar_init(bars.emptyV16(), 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(bars.s_full(s), 1);
       mbar_init(bars.s_free(s), 8);                        // one elected lane per softmax warp
@@ -223,8 +237,13 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
+  if (warp == 0 || warp == 2) {
+    // ---------------- producers: warp 0 the K tiles, warp 2 the V tiles ----------------
+    const bool isk = warp == 0;
+    const int nst = isk ? S::kStK : S::kStV;
+    const uint32_t ring = isk ? S::kOffK8 : S::kOffV8;
+    auto full = [&](int st) { return isk ? bars.fullK8(st) : bars.fullV8(st); };
+    auto empty = [&](int st) { return isk ? bars.emptyK8(st) : bars.emptyV8(st); };
     // page id of slot `lane` of tile jt (-1: not read / invalid); read one tile ahead
     auto page_of = [&](int jt) -> int {
       if (jt >= n_tiles || lane >= ppt) return -1;
@@ -233,7 +252,7 @@ __global__ void __launch_bounds__(kThreads)
       if (max(first, sp.lo) >= min(last, t1)) return -1;
       const int pg = page_at(p, b, first >> bs_sh);
       if (pg < 0 || pg >= p.num_pages) {
-        atomicOr(p.status, TLLM_FLAG_BAD_PAGE);
+        if (isk) atomicOr(p.status, TLLM_FLAG_BAD_PAGE);
         return -1;
       }
       return pg;
@@ -241,44 +260,42 @@ __global__ void __launch_bounds__(kThreads)
     int pg_next = page_of(0);
     int issued = 0;
     for (int j = 0; j < n_tiles; j++) {
-      const int st = j % kStages8;
-      if (j >= kStages8 && !mbar_wait(bars.empty8(st), ((j / kStages8) - 1) & 1, abort)) set_abort_i8(abort, p.status);
+      const int st = j % nst;
+      if (j >= nst && !mbar_wait(empty(st), ((j / nst) - 1) & 1, abort)) set_abort_i8(abort, p.status);
       if (ld_volatile_shared(abort)) break;
       const int pg = pg_next;
       pg_next = page_of(j + 1);
       const int tt = t0 + j * kT;
       const uint32_t mask = __ballot_sync(kFull, pg >= 0);
-      const uint32_t stg = sbase + S::kOff8 + st * S::kStage8;
-      if (lane == 0) mbar_arrive_expect_tx(bars.full8(st), __popc(mask) * (uint32_t)brows * D * 2 * kEsz);
+      const uint32_t stg = sbase + ring + st * S::kStage;
+      if (lane == 0) mbar_arrive_expect_tx(full(st), __popc(mask) * (uint32_t)brows * D * kEsz);
       __syncwarp();
       if (pg >= 0) {
         const int row = (int)(((int64_t)pg * p.Hkv + g) * bs + (bs > kT ? (tt & (bs - 1)) : 0));
-        tma_load_2d(stg + lane * brows * D * kEsz, &kmap, 0, row, bars.full8(st));
-        tma_load_2d(stg + S::kRaw + lane * brows * D * kEsz, &vmap, 0, row, bars.full8(st));
+        tma_load_2d(stg + lane * brows * D * kEsz, isk ? &kmap : &vmap, 0, row, full(st));
       }
-      // scales (quantised caches): lanes 0..15 copy K scales of tokens 4l..4l+3, lanes 16..31
-      // the V scales; every lane arrives once its copy (if any) has landed
+      // scales (quantised caches): lanes 0..15 copy the scales of tokens 4l..4l+3; every lane
+      // arrives once its copy (if any) has landed
       {
         if constexpr (!k16) {
           const int tk = 4 * (lane & 15);
           const int slot = bs < kT ? tk >> bs_sh : 0;
           const int pgl = __shfl_sync(kFull, pg, slot);
-          const bool ok = pgl >= 0;
+          const bool ok = pgl >= 0 && lane < 16;
           const int64_t srow = ok ? ((int64_t)pgl * p.Hkv + g) * bs + ((tt + tk) & (bs - 1)) : 0;
-          const float* src = (lane < 16 ? p.k_scales : p.v_scales) + srow;
-          cp_async16(stg + 2 * S::kRaw + (lane < 16 ? 0 : kT * 4) + tk * 4, src, ok ? 16u : 0u);
+          if (lane < 16) cp_async16(stg + S::kRaw + tk * 4, (isk ? p.k_scales : p.v_scales) + srow, ok ? 16u : 0u);
         }
-        cp_async_arrive_noinc(bars.full8(st));
+        cp_async_arrive_noinc(full(st));
       }
       if (lane == 0) {
-        *reinterpret_cast<volatile uint32_t*>(sm + S::kOff8 + st * S::kStage8 + 2 * S::kRaw + S::kSc) = mask;
-        mbar_arrive(bars.full8(st));
+        *reinterpret_cast<volatile uint32_t*>(sm + ring + st * S::kStage + S::kRaw + S::kScT) = mask;
+        mbar_arrive(full(st));
       }
       issued = j + 1;
     }
     // drain: every issued stage's copies land before the item ends
-    for (int j = max(0, issued - kStages8); j < issued; j++)
-      if (!mbar_wait(bars.full8(j % kStages8), (j / kStages8) & 1, 0u)) set_abort_i8(abort, p.status);
+    for (int j = max(0, issued - nst); j < issued; j++)
+      if (!mbar_wait(full(j % nst), (j / nst) & 1, 0u)) set_abort_i8(abort, p.status);
   } else if (warp == 1 || warp == 3) {
     // ---------------- MMA issuers: warp 1 every QK^T, warp 3 every PV (one thread each) ----------------
     if (lane == 0) {
@@ -286,26 +303,26 @@ __global__ void __launch_bounds__(kThreads)
       if (warp == 1) {
         const uint32_t idqk = idesc_f16(128, kT, 0, 0, 0);   // Q and K in f16
         ok = mbar_wait(bars.q_full(), 0, abort);
-        const uint32_t kt = sbase + S::kOff16;
         for (int j = 0; ok && j < n_tiles; j++) {
-          const int sb = j & 1;
-          if (!mbar_wait(bars.fullK(), j & 1, abort)) { ok = false; break; }
+          const int sb = j & 1;                            // S buffer and f16 K buffer of tile j
+          if (!mbar_wait(bars.fullK16(sb), (j >> 1) & 1, abort)) { ok = false; break; }
           if (j >= 2 && !mbar_wait(bars.s_free(sb), ((j >> 1) - 1) & 1, abort)) { ok = false; break; }
           tc_fence_after();
+          const uint32_t kt = sbase + S::kOff16 + sb * S::kHalf16;
 #pragma unroll
           for (int k = 0; k < D / 16; k++)
             mma_f16_ts(tmem + kColS + 64 * sb, tmem + kColQ + 8 * k,
                        sdesc_sw128(kt + (k >> 2) * S::kAtom + 32 * (k & 3), 16, 1024), idqk, k > 0 ? 1u : 0u);
           mma_commit(bars.s_full(sb));
-          mma_commit(bars.emptyK());
+          mma_commit(bars.emptyK16(sb));
         }
       } else {
         const uint32_t idpv = idesc_f16(128, D, kPParts - 1, 0, 1);   // P and V in f16 (bf16 V: both bf16)
-        const uint32_t vt = sbase + S::kOff16 + S::kHalf16;
+        const uint32_t vt = sbase + S::kOff16 + 2 * S::kHalf16;
         for (int j = 0; ok && j < n_tiles; j++) {
           const int pb = j & 1;
           if (!mbar_wait(bars.p_full(pb), (j >> 1) & 1, abort)) { ok = false; break; }
-          if (!mbar_wait(bars.fullV(), j & 1, abort)) { ok = false; break; }
+          if (!mbar_wait(bars.fullV16(), j & 1, abort)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kT / 16; k++)
@@ -315,7 +332,7 @@ __global__ void __launch_bounds__(kThreads)
                          sdesc_sw128(sbase + S::kOffP + pb * S::kPBuf + part * S::kPPart + 32 * k, 16, 1024),
                          sdesc_sw128(vt + 2048 * k, S::kAtom, 1024), idpv, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
           mma_commit(bars.pv_done(pb));
-          mma_commit(bars.emptyV());
+          mma_commit(bars.emptyV16());
         }
       }
       if (!ok) set_abort_i8(abort, p.status);
@@ -327,36 +344,43 @@ __global__ void __launch_bounds__(kThreads)
     // (an aligned barrier) converged
     __syncwarp();
   } else if (warp >= 12) {
-    // ---------------- converters: a staged tile -> f16 tiles, scales and mask ----------------
-    // Warps 12..15 widen each tile's K half, then its V half, all four warps on each: K(j) once
-    // the QK^T of tile j - 1 is done, V(j) once the PV of tile j - 1 is done. Widening K(j + 1)
-    // then overlaps the PV of tile j, which the V half of tile j + 1 waits for.
+    // ---------------- converters: staged tiles -> f16 tiles, scales and mask ----------------
+    // Warps 12..15 widen, all four on each, K(0), then for every later step j K(j) and V(j - 1),
+    // then the last V: K(j) into f16 K buffer j % 2 once the QK^T of tile j - 2 is done, V(j)
+    // into the f16 V buffer once the PV of tile j - 1 is done. K thus runs a tile ahead of V,
+    // and the QK^T of tile j + 1 goes out while the softmax of tile j runs.
     const int ct = tid - 384;                              // 0..127
     constexpr int kEpc = 16 / kEsz;                        // elements per 16-byte chunk
     constexpr int kChunksPerRow = D / kEpc, kPer = kT * kChunksPerRow / 128;
     float* xc = xf + 1024;                                 // the converter warps' tile maxima (bf16 K)
-    for (int j = 0; j < n_tiles; j++) {
-      const int st = j % kStages8;
-      if (!mbar_wait(bars.full8(st), (j / kStages8) & 1, abort)) set_abort_i8(abort, p.status);
-      const uint8_t* src = sm + S::kOff8 + st * S::kStage8;
-      const uint32_t dst = sbase + S::kOff16;
-      const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + 2 * S::kRaw + S::kSc);
-      const int tt = t0 + j * kT;
-      // is row t of this tile a token the split reads? (a slot past the context, before the
-      // window, or of a page not loaded holds stale or poisoned bytes)
-      auto read_tok = [&](int t) -> bool {
-        const int slot = bs < kT ? t >> bs_sh : 0;
-        return ((pmask8 >> slot) & 1) && tt + t >= vlo && tt + t < t1;
-      };
+    for (int step = 0; step <= n_tiles; step++) {
 #pragma unroll
-      for (int which = 0; which < 2; which++) {
+      for (int which = 0; which < 2; which++) {            // 0: K of tile step, 1: V of tile step - 1
+        const int j = step - which;
+        if (which == 0 ? j >= n_tiles : j < 0) continue;
+        const int stk = j % S::kStK, stv = j % S::kStV;
+        const uint8_t* srck = sm + S::kOffK8 + stk * S::kStage;
+        const uint8_t* srcv = sm + S::kOffV8 + stv * S::kStage;
+        if (which == 0) {
+          if (!mbar_wait(bars.fullK8(stk), (j / S::kStK) & 1, abort)) set_abort_i8(abort, p.status);
+          if (!mbar_wait(bars.fullV8(stv), (j / S::kStV) & 1, abort)) set_abort_i8(abort, p.status);
+        }
+        const uint8_t* src = which == 0 ? srck : srcv;     // (the K stage is not read for V: it may hold tile j + 2)
+        const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + S::kRaw + S::kScT);
+        const int tt = t0 + j * kT;
+        // is row t of this tile a token the split reads? (a slot past the context, before the
+        // window, or of a page not loaded holds stale or poisoned bytes)
+        auto read_tok = [&](int t) -> bool {
+          const int slot = bs < kT ? t >> bs_sh : 0;
+          return ((pmask8 >> slot) & 1) && tt + t >= vlo && tt + t < t1;
+        };
         // this thread's chunks of the operand, loaded before anything is converted (their
         // latencies overlap)
         uint4 w[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
           const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
-          w[i] = *reinterpret_cast<const uint4*>(src + which * S::kRaw + (t * D + d0) * kEsz);
+          w[i] = *reinterpret_cast<const uint4*>(src + (t * D + d0) * kEsz);
         }
         // A bf16 K tile enters f16 scaled by 2^e, e from the largest |x| the split reads in it,
         // so that this maximum lies in [2^13, 2^14): every element within 2^-27 of it converts to
@@ -390,14 +414,13 @@ __global__ void __launch_bounds__(kThreads)
           // largest |V scale|. The K scales leave here multiplied by the softmax scale in log2
           // units, so that a score reaches the softmax as one product with the query row's
           // power of two, which is exact. Slot j % 4 last held tile j - 4, whose softmax is
-          // over: tile j's copies were issued after the converters released tile j - 3's stage,
-          // which they did after widening V(j - 3), after the PV of tile j - 4, which waited for
-          // that softmax.
-          // A token the split does not read gets zero scales (its staged scale may be stale or
-          // NaN), so that the softmax's P x V-scale product is 0 there without a select.
+          // over: V(j - 3), widened two steps before this one, waited for the PV of tile j - 4,
+          // which waited for that softmax. A token the split does not read gets zero scales (its
+          // staged scale may be stale or NaN), so that the softmax's P x V-scale product is 0
+          // there without a select.
           float scv;
           if constexpr (k16) scv = ct < kT ? __int_as_float((127 - e) << 23) : 1.f;   // 2^-e for K
-          else scv = reinterpret_cast<const float*>(src + 2 * S::kRaw)[ct];
+          else scv = reinterpret_cast<const float*>((ct < kT ? srck : srcv) + S::kRaw)[ct & (kT - 1)];
           if (!read_tok(ct & (kT - 1))) scv = 0.f;
           uint8_t* meta = sm + S::kOffMeta + (j & 3) * S::kMeta;
           reinterpret_cast<float*>(meta)[ct] = ct < kT ? scv * p.scale_log2 : scv;
@@ -407,9 +430,12 @@ __global__ void __launch_bounds__(kThreads)
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
         }
-        // the one f16 stage's K (V) half is free once the previous tile's QK^T (PV) is done
-        if (j >= 1 && !mbar_wait(which == 0 ? bars.emptyK() : bars.emptyV(), (j - 1) & 1, abort))
+        // f16 K buffer j % 2 is free once the QK^T of tile j - 2 is done; the V buffer once the
+        // PV of tile j - 1 is done
+        if (which == 0 ? (j >= 2 && !mbar_wait(bars.emptyK16(j & 1), ((j >> 1) - 1) & 1, abort))
+                       : (j >= 1 && !mbar_wait(bars.emptyV16(), (j - 1) & 1, abort)))
           set_abort_i8(abort, p.status);
+        const uint32_t dst = sbase + S::kOff16 + (which == 0 ? (j & 1) : 2) * S::kHalf16;
         const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
         const float emul = __int_as_float((e + 127) << 23);
 #pragma unroll
@@ -420,7 +446,7 @@ __global__ void __launch_bounds__(kThreads)
           // the softmax selects -inf for those tokens' scores.) Int8 codes are always finite.
           const bool ok = kKv == kKvI8 || which == 0 || read_tok(t);
           const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-          const uint32_t base = dst + which * S::kHalf16 + (d0 >> 6) * S::kAtom;
+          const uint32_t base = dst + (d0 >> 6) * S::kAtom;
           const uint32_t byte = (d0 & 63) * 2;
           if constexpr (!k16) {
             uint32_t h[8];
@@ -460,14 +486,18 @@ __global__ void __launch_bounds__(kThreads)
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(which == 0 ? bars.fullK() : bars.fullV());
+        if (lane == 0) {
+          mbar_arrive(which == 0 ? bars.fullK16(j & 1) : bars.fullV16());
+          mbar_arrive(which == 0 ? bars.emptyK8(stk) : bars.emptyV8(stv));
+        }
       }
-      if (lane == 0) mbar_arrive(bars.empty8(st));
     }
-    // the releases of the f16 stage by the last tile's MMAs (asynchronous tcgen05.commit
+    // the releases of the f16 buffers by the last tiles' MMAs (asynchronous tcgen05.commit
     // arrivals) must have landed before the next item re-initialises the barriers
-    if (!mbar_wait(bars.emptyK(), (n_tiles - 1) & 1, abort)) set_abort_i8(abort, p.status);
-    if (!mbar_wait(bars.emptyV(), (n_tiles - 1) & 1, abort)) set_abort_i8(abort, p.status);
+    const int nl = n_tiles - 1;
+    if (!mbar_wait(bars.emptyK16(nl & 1), (nl >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+    if (nl >= 1 && !mbar_wait(bars.emptyK16((nl - 1) & 1), ((nl - 1) >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+    if (!mbar_wait(bars.emptyV16(), nl & 1, abort)) set_abort_i8(abort, p.status);
   } else if (warp >= 4) {
     // ---------------- softmax: two threads per packed row r (TMEM lane), one per token half ----------------
     const int hh = (warp - 4) >> 2;                        // token half (0: tokens 0..31, 1: 32..63)
