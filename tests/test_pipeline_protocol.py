@@ -1,0 +1,146 @@
+"""A model of the widening tensor-core kernel's mbarrier protocol, run under random schedules.
+
+Each role of the kernel (the K and V producers, the converter warps, the two MMA issuers, the
+softmax warps) is a sequence of waits on, and arrivals at, the kernel's mbarriers in the order
+the CUDA source issues them; the asynchronous arrivals (TMA copies landing, tcgen05.commit)
+happen at random later moments. An mbarrier wait names a phase by its parity only, so the
+protocol is correct only if every wait for phase k starts when the barrier has completed k or
+k + 1 phases and no barrier completes phase k + 2 while a wait for phase k is still pending.
+The test checks that, and that every schedule runs to its end, for 1 to 12 tiles per item;
+and that the check catches a planted mistake.
+"""
+import random
+
+import pytest
+
+SK, SV = 2, 3          # staging ring depths: K, V
+
+
+class Bar:
+    def __init__(self, name):
+        self.name, self.done = name, 0
+
+    def complete(self, waits):
+        for (bar, k, who) in waits:
+            if bar is self and k < self.done:
+                raise AssertionError(f"{self.name}: phase {self.done} completes while {who} still waits phase {k}")
+        self.done += 1
+
+
+def roles(n, rnd, rescale_p, skip_v_wait=False):
+    def prod(name, depth):
+        for j in range(n):
+            st = j % depth
+            if j >= depth:
+                yield ("wait", f"e{name}8{st}", j // depth - 1)
+            yield ("async", [f"f{name}8{st}"])
+        for j in range(max(0, n - depth), n):
+            yield ("wait", f"f{name}8{j % depth}", j // depth)
+
+    def conv():
+        for step in range(n + 1):
+            if step < n:
+                j = step
+                yield ("wait", f"fK8{j % SK}", j // SK)
+                yield ("wait", f"fV8{j % SV}", j // SV)
+                yield ("arrive", f"meta{j % 4}")
+                if j >= 2:
+                    yield ("wait", f"eK16{j & 1}", (j >> 1) - 1)
+                yield ("arrive", f"fK16{j & 1}")
+                yield ("arrive", f"eK8{j % SK}")
+            if step >= 1:
+                j = step - 1
+                if j >= 1 and not skip_v_wait:
+                    yield ("wait", "eV16", j - 1)
+                yield ("arrive", "fV16")
+                yield ("arrive", f"eV8{j % SV}")
+        yield ("wait", f"eK16{(n - 1) & 1}", (n - 1) >> 1)
+        if n >= 2:
+            yield ("wait", f"eK16{(n - 2) & 1}", (n - 2) >> 1)
+        yield ("wait", "eV16", n - 1)
+
+    def qk():
+        yield ("wait", "q", 0)
+        for j in range(n):
+            yield ("wait", f"fK16{j & 1}", j >> 1)
+            if j >= 2:
+                yield ("wait", f"sfree{j & 1}", (j >> 1) - 1)
+            yield ("async", [f"sfull{j & 1}", f"eK16{j & 1}"])
+
+    def pv():
+        for j in range(n):
+            yield ("wait", f"pfull{j & 1}", j >> 1)
+            yield ("wait", "fV16", j)
+            yield ("async", [f"pv{j & 1}", "eV16"])
+
+    def soft():
+        yield ("arrive", "q")
+        last = -1
+        for j in range(n):
+            last = j
+            yield ("wait", f"meta{j % 4}", j >> 2)
+            yield ("wait", f"sfull{j & 1}", j >> 1)
+            yield ("arrive", f"sfree{j & 1}")
+            if j >= 2:
+                yield ("wait", f"pv{j & 1}", (j >> 1) - 1)
+            if j >= 1 and rnd.random() < rescale_p:       # the O rescale waits for the last PV
+                yield ("wait", f"pv{(j - 1) & 1}", (j - 1) >> 1)
+            yield ("arrive", f"pfull{j & 1}")
+        if last >= 1:
+            yield ("wait", f"pv{(last - 1) & 1}", (last - 1) >> 1)
+        if last >= 0:
+            yield ("wait", f"pv{last & 1}", last >> 1)
+
+    return {"prodK": prod("K", SK), "prodV": prod("V", SV), "conv": conv(), "qk": qk(), "pv": pv(),
+            "soft": soft()}
+
+
+def run(n, seed, rescale_p=0.3, skip_v_wait=False):
+    rnd = random.Random(seed)
+    bars = {}
+
+    def bar(name):
+        if name not in bars:
+            bars[name] = Bar(name)
+        return bars[name]
+
+    actors = roles(n, rnd, rescale_p, skip_v_wait)
+    cur = {k: next(g, None) for k, g in actors.items()}
+    pending = []
+    for _ in range(200000):
+        waits = [(bar(a[1]), a[2], k) for k, a in cur.items() if a and a[0] == "wait"]
+        ready = [k for k, a in cur.items() if a is not None and (a[0] != "wait" or bar(a[1]).done > a[2])]
+        choices = ready + (["async"] if pending else [])
+        if not choices:
+            assert all(a is None for a in cur.values()), f"deadlock with {n} tiles: {cur}"
+            return
+        c = rnd.choice(choices)
+        if c == "async":
+            bar(pending.pop(rnd.randrange(len(pending)))).complete(waits)
+            continue
+        a = cur[c]
+        if a[0] == "wait":
+            assert bar(a[1]).done <= a[2] + 1, f"{c} waits {a[1]} phase {a[2]} after {bar(a[1]).done} phases"
+        elif a[0] == "arrive":
+            bar(a[1]).complete(waits)
+        else:
+            pending.extend(a[1])
+        cur[c] = next(actors[c], None)
+        nxt = cur[c]
+        if nxt is not None and nxt[0] == "wait":
+            assert bar(nxt[1]).done >= nxt[2], f"{c} waits {nxt[1]} phase {nxt[2]} before phase {nxt[2] - 1} completed"
+    raise AssertionError("schedule did not end")
+
+
+@pytest.mark.parametrize("n", list(range(1, 13)))
+def test_widening_kernel_barrier_protocol(n):
+    for seed in range(100):
+        run(n, 7919 * n + seed)
+
+
+def test_the_protocol_check_catches_a_missing_wait():
+    """Widening V without waiting for the previous PV lets the V buffer's barrier run two
+    phases ahead of the PV issuer's wait."""
+    with pytest.raises(AssertionError):
+        for seed in range(200):
+            run(6, seed, skip_v_wait=True)
