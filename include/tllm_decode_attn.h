@@ -281,10 +281,9 @@ const char* tllm_status_string(tllm_status status);
 
 /*
  * tllm_decode_attn_splitkv without a caller workspace. This entry point has no counterpart
- * in the papers; it exists for callers that cannot allocate device memory. Examples are
- * code running inside a stream capture in the global capture mode (where cudaMalloc is an
- * illegal call), engines that reserve all device memory for their own pools, and plugin
- * hosts that pass kernels only their tensors.
+ * in the papers; it exists for callers that cannot allocate device memory, for example
+ * engines that reserve all device memory for their own pools, and plugin hosts that pass
+ * kernels only their tensors.
  *   - The split records live in a library-owned device array of
  *     TLLM_NOALLOC_SCRATCH_BYTES bytes. Every GPU that loads the library holds that array
  *     until the process exits.
@@ -298,8 +297,7 @@ const char* tllm_status_string(tllm_status status);
  *     that word afterwards.
  *   - All calls on a device share the one array, and it keeps the last call's contents.
  *     Calls that overlap on the GPU (unordered streams) race on it.
- *   - The first call on each device looks up the array's device address. Make that call
- *     before any stream capture begins.
+ *   - The first call on each device looks up the array's device address.
  */
 tllm_status tllm_decode_attn_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                              const int32_t* block_table, const int32_t* context_lens,

@@ -2,8 +2,6 @@
 // device memory.
 //
 // Some callers cannot call cudaMalloc. Examples:
-//   - code running while a stream is being captured in the global capture mode, where an
-//     allocation is an illegal call;
 //   - serving engines that reserve all of device memory up front for their KV-cache pool
 //     and hand kernels no allocator;
 //   - plugin hosts that expose only the tensors of a call.
@@ -17,8 +15,7 @@
 //   - Every call on a device shares the one array, which keeps the last call's contents.
 //     Calls whose work overlaps on the GPU (different streams, no ordering between them)
 //     race on it; order them on one stream or with events.
-//   - The first call on each device looks up the array's device address. Make that first
-//     call before any stream capture begins.
+//   - The first call on each device looks up the array's device address.
 #include <mutex>
 
 #include "common.cuh"

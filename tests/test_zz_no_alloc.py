@@ -1,9 +1,9 @@
 """The allocation-free entry point, for callers that cannot allocate device memory.
 
 tllm_decode_attn_splitkv_noalloc keeps its split records in the library's own device
-array instead of a caller workspace. Callers that cannot allocate are, for example, code
-inside a stream capture in the global capture mode, engines that reserve all of device
-memory for their own pools, and plugin hosts that pass only tensors.
+array instead of a caller workspace. Callers that cannot allocate are, for example, engines
+that reserve all of device memory for their own pools, and plugin hosts that pass only
+tensors.
 
 The test calls it through the C ABI twice in a row, on two different workloads. Before the
 second call the array is filled with stale records (NaN outputs, other log-sum-exps) by a
