@@ -258,7 +258,25 @@ def test_partial_records_match_oracle_partials(kernel, rec):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_device_data_faults_set_status_and_stay_finite(kernel):
-    wl = W.mtp4_fp8_long(batch=3, ctx=1000)
+    _check_device_data_faults(W.mtp4_fp8_long(batch=3, ctx=1000), kernel)
+
+
+@pytest.mark.parametrize("wl,kernel", [
+    (W.verify16_int8().replace(ctx=[1000, 1000, 1000]), B.TLLM_KERNEL_TC_I8),
+    (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, Hq=32, Hkv=4, Lq=4, window=0, sinks=False),
+     B.TLLM_KERNEL_TC_I8),
+    (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, Hq=32, Hkv=2, Lq=1, D=256, window=0, sinks=False),
+     B.TLLM_KERNEL_SIMT),
+    (W.single_decode().replace(ctx=[1000] * 3), B.TLLM_KERNEL_SIMT),
+    (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, window=0, sinks=False), B.TLLM_KERNEL_TC_B16),
+])
+def test_device_data_faults_in_every_kernel(wl, kernel):
+    """A clamped context length and out-of-range page ids (too large, negative) in the widening,
+    CUDA-core (one and several row blocks) and 16-bit kernels: flagged, masked, finite."""
+    _check_device_data_faults(wl, kernel)
+
+
+def _check_device_data_faults(wl, kernel):
     inp = _inputs(wl, 13, poison=False)
     plan = plan_for(wl, kernel, 2, num_pages=inp.num_pages)
     ws = poisoned_workspace(plan)
@@ -697,6 +715,10 @@ def _contiguous(inp):
     (W.window_sink_bf16(batch=3).replace(ctx=[6000, 4097, 17]), B.TLLM_KERNEL_TC_B16),
     (W.single_decode().replace(ctx=[2048, 300]), B.TLLM_KERNEL_SIMT),
     (W.single_decode().replace(ctx=[2048, 300]), B.TLLM_KERNEL_GENERIC),
+    (W.window_sink_bf16(batch=2).replace(ctx=[3000, 650], Hq=32, Hkv=4, Lq=4), B.TLLM_KERNEL_TC_I8),
+    (W.window_sink_bf16(batch=2).replace(ctx=[3000, 650], Hq=32, Hkv=4, Lq=4, D=64, kv_dtype="f16"),
+     B.TLLM_KERNEL_TC_I8),
+    (W.window_sink_bf16(batch=2).replace(ctx=[3000, 650], Hq=32, Hkv=2, Lq=2, D=256), B.TLLM_KERNEL_SIMT),
 ])
 def test_contiguous_cache_without_block_table(wl, kernel):
     """block_table = NULL: request b's block i is page b * max_blocks + i. The result equals
