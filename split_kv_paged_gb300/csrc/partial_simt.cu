@@ -190,6 +190,14 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.x, b = u / p.Hkv, g = u % p.Hkv, split = blockIdx.y;
   const int r0 = blockIdx.z * RM;                          // first packed row of this CTA's block
+  // the block-table entries this split reads when its request has the full length (64 of them
+  // from the split's share of the row), pulled into L2 while the context length is in flight:
+  // the page-id loads that follow it then hit L2
+  if (p.block_table && tid < 2) {
+    const int per = (p.max_blocks + p.num_splits - 1) / p.num_splits;
+    const int first = min(split * per + 32 * tid, p.max_blocks - 1);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.block_table + (int64_t)b * p.max_blocks + first));
+  }
   const int raw_ctx = p.context_lens[b];
   const int ctx = clamp_ctx(raw_ctx, p.max_ctx);
   if (raw_ctx != ctx && tid == 0 && split == 0 && r0 == 0) atomicOr(p.status, TLLM_FLAG_CTX_CLAMPED);
