@@ -3,6 +3,9 @@
 // plain GQA (R = G) is this shape; with so few rows per KV head a tensor-core tile would be
 // mostly padding, and the kernel is bound by the HBM stream alone.
 //
+// It also reads a dimension-major ("transposed") V cache, [num_pages, Hkv, D, bs]: V tiles are
+// staged dimension by dimension (16-byte copies of a page row) and gathered per token.
+//
 // One CTA = one (request, kv head, split, block of 8 packed rows), 256 threads; with at most 8
 // rows there is one row block and each KV byte of the split is read once (GQA packing: "split
 // packed-Q8 verifier KV scans", hipfire PR #760, Summary). More rows (the shapes no tensor-core
@@ -18,6 +21,8 @@
 //            over the tokens it sees (tiny-llm PR #11: per-split online (m, l, acc)).
 //   Merge:   the groups' (m, l, acc) are merged once, through shared memory, into the
 //            split's normalised record (or the final output when the request has one split).
+#include <type_traits>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -134,6 +139,21 @@ struct Row8<int8_t> {
 };
 
 // Eight or sixteen consecutive elements of a cache row, widened to fp32.
+// one element of the cache type, widened to fp32
+template <typename KT>
+__device__ __forceinline__ float elt_f32(const uint8_t* s) {
+  if constexpr (std::is_same<KT, __half>::value) return __half2float(*reinterpret_cast<const __half*>(s));
+  else if constexpr (std::is_same<KT, __nv_bfloat16>::value)
+    return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(s) << 16);
+  else if constexpr (std::is_same<KT, int8_t>::value) return (float)*reinterpret_cast<const int8_t*>(s);
+  else {
+    uint32_t h2;
+    const uint16_t pair = *s;                              // the code in the low byte
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    return __half2float(*reinterpret_cast<const __half*>(&h2));
+  }
+}
+
 template <typename KT, int N>
 __device__ __forceinline__ void load_row(const uint8_t* s, float (&x)[N]) {
   static_assert(N % 8 == 0, "whole 8-element pieces");
@@ -161,6 +181,14 @@ struct Shape {
   static constexpr int kStageBytes = 2 * kTile * kRowStride + (kScaled ? 2 * kTile * 4 : 0);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kRingBytes = kStages * kStageBytes;
+  // dimension-major V in shared memory: D rows of the tile's tokens (kTile elements), the
+  // 16-byte chunks of row d placed at chunk ^ ((d / 8) % kDmChunks), so that the lanes of a
+  // token group, which read dims 8 li .. 8 li + 7 of one token, reach different bank groups
+  static constexpr int kElt = Row8<KT>::kBytes / 8;
+  static constexpr int kDmRow = kTile * kElt;                       // bytes of one dim's row
+  static constexpr int kDmChunks = kDmRow / 16;                     // 16-byte chunks per row
+  static_assert(D * kDmRow <= kTile * kRowStride, "a dimension-major V tile fits the V stage");
+  static_assert(D * kDmChunks == kTile * kChunksPerRow, "same copy count as the token-major tile");
   static_assert(kTpg >= 1 && kTile % kGroups == 0, "tile");
   static_assert(kRingBytes >= kMaxSplits * 8 * 4, "the fused merge's weights (splits x rows) fit in the ring");
   static_assert(kTile * kChunksPerRow % kThreads == 0, "copy split");
@@ -179,7 +207,9 @@ __host__ __device__ constexpr int simt_smem_bytes() {
   return (ring > merge ? ring : merge) + kPgSlots * 32 * 4 + 64;
 }
 
-template <typename KT, int D, int RM>
+// kVdm: the V cache is dimension-major (a separate instance, so the token-major one compiles as
+// without it)
+template <typename KT, int D, int RM, bool kVdm>
 __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel(Params p) {
   using S = Shape<KT, D, RM>;
   if (threadIdx.x == 0) pdl_launch_dependents();
@@ -268,7 +298,19 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
       const bool ok = jt < n_tiles && pg >= 0 && t >= vlo && t < t1;
       const int64_t row = ok ? ((int64_t)pg * p.Hkv + g) * bs + (t & (bs - 1)) : 0;
       cp_async16_zfill(kdst + tok * S::kRowStride + off, kc + row * S::kRowBytes + off, ok);
-      cp_async16_zfill(vdst + tok * S::kRowStride + off, vc + row * S::kRowBytes + off, ok);
+      if constexpr (!kVdm) {
+        cp_async16_zfill(vdst + tok * S::kRowStride + off, vc + row * S::kRowBytes + off, ok);
+      } else {
+        // dimension-major V: chunk c is 16 bytes of dim d's page row, tokens tl .. tl + 16 / kElt
+        // - 1 of the tile (on one page: bs is a multiple of 16 / kElt); a chunk any of whose
+        // tokens the split reads is copied whole, the rest zero-filled
+        constexpr int kTpc = 16 / S::kElt;
+        const int d = c / S::kDmChunks, cc = c % S::kDmChunks, tl = cc * kTpc, tv = tt + tl;
+        const int pgv = pg_s[(jt % kPgSlots) * 32 + (tl >> bs_sh)];
+        const bool okv = jt < n_tiles && pgv >= 0 && tv + kTpc > vlo && tv < t1;
+        const int64_t src = okv ? ((((int64_t)pgv * p.Hkv + g) * D + d) * bs + (tv & (bs - 1))) * S::kElt : 0;
+        cp_async16_zfill(vdst + d * S::kDmRow + ((cc ^ ((d >> 3) & (S::kDmChunks - 1))) << 4), vc + src, okv);
+      }
     }
     if constexpr (S::kScaled) {
       const uint32_t sdst = vdst + kTile * S::kRowStride;   // [K scales | V scales], kTile each
@@ -327,6 +369,24 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
     for (int i = 0; i < ppt; i++) pages_ok = pages_ok && pgt[i] >= 0;
     const bool whole = pages_ok && tt >= vlo && tt + kTile <= t1 && tt + kTile - 1 <= pos_lo &&
                        (p.window <= 0 || tt > ctx - 1 - p.window);
+    if constexpr (kVdm) {
+      // V of the tokens the split does not read (before the window, past the length, on a page
+      // not loaded) may hold stale or poisoned values in a partly read chunk: zero them before
+      // the PV reads the tile (their p is 0, but 0 x NaN is not 0)
+      if (!(pages_ok && tt >= vlo && tt + kTile <= t1)) {
+        uint8_t* vw = smem + st * S::kStageBytes + kTile * S::kRowStride;
+        for (int idx = tid; idx < D * kTile; idx += kThreads) {
+          const int d = idx / kTile, tl = idx % kTile, t = tt + tl;
+          if (!(t >= vlo && t < t1 && pgt[kTile >= bs ? tl >> bs_sh : 0] >= 0)) {
+            uint8_t* e = vw + d * S::kDmRow + ((((tl * S::kElt) >> 4) ^ ((d >> 3) & (S::kDmChunks - 1))) << 4) +
+                         ((tl * S::kElt) & 15);
+            if constexpr (S::kElt == 2) *reinterpret_cast<uint16_t*>(e) = 0;
+            else *e = 0;
+          }
+        }
+        __syncthreads();
+      }
+    }
     float sk[S::kTpg];                                        // this lane's row: scores of the group's tokens
 #pragma unroll
     for (int k = 0; k < S::kTpg; k++) {
@@ -376,7 +436,16 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
     for (int k = 0; k < S::kTpg; k++) {
       const int tok = grp * S::kTpg + k;
       float vx[S::kDpl];
-      load_row<KT, S::kDpl>(vs_tile + tok * S::kRowStride + li * (S::kRowBytes / S::kLpt), vx);
+      if constexpr (!kVdm) {
+        load_row<KT, S::kDpl>(vs_tile + tok * S::kRowStride + li * (S::kRowBytes / S::kLpt), vx);
+      } else {
+        // dims 8 li .. 8 li + 7 of token tok: one element from each of 8 dim rows (their chunk
+        // placed at chunk ^ li)
+        const uint8_t* vr = vs_tile + ((((tok * S::kElt) >> 4) ^ (li & (S::kDmChunks - 1))) << 4) +
+                            ((tok * S::kElt) & 15);
+#pragma unroll
+        for (int e = 0; e < S::kDpl; e++) vx[e] = elt_f32<KT>(vr + (S::kDpl * li + e) * S::kDmRow);
+      }
       // masked tokens have p = 0; their scale may be anything (NaN included), so it is
       // selected away rather than multiplied
       const float vsc = S::kScaled ? sc[kTile + tok] : 1.f;
@@ -445,33 +514,33 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
   }
 }
 
-template <typename KT, int D, int RM>
+template <typename KT, int D, int RM, bool kVdm>
 cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
   constexpr int smem = simt_smem_bytes<KT, D, RM>();
-  const void* f = reinterpret_cast<const void*>(&partial_simt_kernel<KT, D, RM>);
+  const void* f = reinterpret_cast<const void*>(&partial_simt_kernel<KT, D, RM, kVdm>);
   cudaError_t e = set_smem_attr(f, smem);
   if (e != cudaSuccess) return e;
-  partial_simt_kernel<KT, D, RM><<<grid, kThreads, smem, stream>>>(p);
+  partial_simt_kernel<KT, D, RM, kVdm><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <typename KT, int RM>
+template <typename KT, int RM, bool kVdm>
 cudaError_t launch_d(const Params& p, dim3 grid, cudaStream_t stream) {
   switch (p.D) {
-    case 64: return launch_one<KT, 64, RM>(p, grid, stream);
-    case 128: return launch_one<KT, 128, RM>(p, grid, stream);
-    case 256: return launch_one<KT, 256, RM>(p, grid, stream);
+    case 64: return launch_one<KT, 64, RM, kVdm>(p, grid, stream);
+    case 128: return launch_one<KT, 128, RM, kVdm>(p, grid, stream);
+    case 256: return launch_one<KT, 256, RM, kVdm>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <int RM>
+template <int RM, bool kVdm>
 cudaError_t launch_kt(const Params& p, dim3 grid, cudaStream_t stream) {
   switch (p.kv_dtype) {
-    case TLLM_F16: return launch_d<__half, RM>(p, grid, stream);
-    case TLLM_BF16: return launch_d<__nv_bfloat16, RM>(p, grid, stream);
-    case TLLM_FP8_E4M3: return launch_d<__nv_fp8_e4m3, RM>(p, grid, stream);
-    case TLLM_INT8: return launch_d<int8_t, RM>(p, grid, stream);
+    case TLLM_F16: return launch_d<__half, RM, kVdm>(p, grid, stream);
+    case TLLM_BF16: return launch_d<__nv_bfloat16, RM, kVdm>(p, grid, stream);
+    case TLLM_FP8_E4M3: return launch_d<__nv_fp8_e4m3, RM, kVdm>(p, grid, stream);
+    case TLLM_INT8: return launch_d<int8_t, RM, kVdm>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -482,7 +551,11 @@ bool simt_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   const bool kv_ok = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16 || d.kv_dtype == TLLM_FP8_E4M3 ||
                      d.kv_dtype == TLLM_INT8;
-  return kv_ok && d.v_layout == TLLM_V_TOKEN_MAJOR && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) &&
+  // a transposed V cache: a 16-byte copy must hold tokens of one page (16-bit: bs >= 8; 8-bit:
+  // bs >= 16)
+  const bool kv16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
+  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || (d.v_layout == TLLM_V_DIM_MAJOR && (kv16 || bs >= 16));
+  return kv_ok && v_ok && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) &&
          rows >= 1 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128);
 }
 
@@ -494,9 +567,11 @@ bool simt_pointers_ok(const Params& p) {
 }
 
 cudaError_t launch_partial_simt(const Params& p, cudaStream_t stream) {
-  const int rm = p.R <= 4 ? 4 : 8;                          // rows per CTA
+  // rows per CTA (a transposed V cache: always 8, one instance per cache type and head_dim)
+  const int rm = p.R <= 4 && !p.v_dim_major ? 4 : 8;
   dim3 grid(p.B * p.Hkv, p.num_splits, (p.R + rm - 1) / rm);
-  return rm == 4 ? launch_kt<4>(p, grid, stream) : launch_kt<8>(p, grid, stream);
+  if (p.v_dim_major) return launch_kt<8, true>(p, grid, stream);
+  return rm == 4 ? launch_kt<4, false>(p, grid, stream) : launch_kt<8, false>(p, grid, stream);
 }
 
 }  // namespace tllm

@@ -765,6 +765,35 @@ def test_dim_major_v_cache(bs, kernel):
 
 
 
+@pytest.mark.parametrize("kv_dtype,q_dtype,D,bs,Hq,Hkv,Lq", [
+    ("f16", "f16", 64, 8, 14, 2, 1), ("bf16", "bf16", 128, 16, 32, 8, 1), ("bf16", "bf16", 256, 32, 32, 2, 1),
+    ("i8", "bf16", 256, 16, 24, 4, 16), ("e4m3", "bf16", 64, 64, 16, 1, 4), ("i8", "f16", 128, 128, 8, 2, 2),
+    ("f16", "bf16", 128, 16, 12, 4, 3),
+])
+def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
+    """The pipelined CUDA-core kernel on a transposed V cache (AUTO's choice for every shape the
+    FP8 tensor-core kernel does not take): every cache type and head_dim, pages of 8 to 128
+    tokens, one row block and several, with a window, sinks, ragged lengths and poisoned tails
+    and pages."""
+    wl = W.verify16_int8().replace(ctx=[3000, 700, 65, 9], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, bs=bs, kv_dtype=kv_dtype,
+                                   q_dtype=q_dtype, window=900, sinks=True, extra_pages=4,
+                                   kv_std=0.5 if kv_dtype == "e4m3" else 1.0)
+    inp = _inputs(wl, 300 + D + bs + Hq)
+    ref, _ = oracle_out(inp)
+    v_dm = inp.v_cache.transpose(-1, -2).contiguous()
+    for S in (1, 3):
+        desc = B.desc_for(wl, B.TLLM_KERNEL_AUTO, num_pages=inp.num_pages, v_layout=B.TLLM_V_DIM_MAJOR)
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        assert plan.kernel == B.TLLM_KERNEL_SIMT
+        ws = poisoned_workspace(plan)
+        out = new_out(wl)
+        B.tllm_decode_attn_splitkv(inp.q, inp.k_cache, v_dm, inp.block_table, inp.context_lens, wl.Lq,
+                                   inp.kv_scales, inp.sinks, wl.window, S, ws, out)
+        torch.cuda.synchronize()
+        assert not (B.tllm_decode_attn_read_status(ws) & B.TLLM_FLAG_TIMEOUT)
+        assert_close(out, ref, wl.kv_dtype, f"dim-major V simt {kv_dtype} D{D} bs{bs} S{S}")
+
+
 # --- 16-bit split records -------------------------------------------------------------
 
 @pytest.mark.parametrize("rec", [B.TLLM_RECORD_BF16, B.TLLM_RECORD_F16])
