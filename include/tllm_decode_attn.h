@@ -138,6 +138,10 @@ typedef struct {
   tllm_v_layout v_layout;            /* TLLM_V_TOKEN_MAJOR unless the V cache is transposed */
   tllm_record_type record_type;      /* TLLM_RECORD_F32 unless 16-bit split records are wanted */
   tllm_combine_mode combine_mode;    /* TLLM_COMBINE_KERNEL unless the fused merge is wanted */
+  int32_t test_stall;                /* 0. 1 (failure-detection tests only): the widening tensor-core
+                                        kernel's QK^T issuer issues nothing, so the pipeline's bounded
+                                        waits run out; the call sets TLLM_FLAG_TIMEOUT and its output
+                                        is not valid. Other kernels ignore it. */
 } tllm_decode_attn_desc;
 
 /* Host POD produced by tllm_decode_attn_plan; copy it freely. */

@@ -49,7 +49,7 @@ class tllm_decode_attn_desc(ctypes.Structure):
                 ("max_blocks_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("softmax_scale", ctypes.c_float), ("kernel", ctypes.c_int), ("v_layout", ctypes.c_int),
-                ("record_type", ctypes.c_int), ("combine_mode", ctypes.c_int)]
+                ("record_type", ctypes.c_int), ("combine_mode", ctypes.c_int), ("test_stall", ctypes.c_int32)]
 
 
 class tllm_decode_attn_plan_t(ctypes.Structure):

@@ -37,6 +37,7 @@ tllm_status check_desc(const tllm_decode_attn_desc* d) {
   if (d->record_type != TLLM_RECORD_F32 && d->record_type != TLLM_RECORD_BF16 && d->record_type != TLLM_RECORD_F16)
     return TLLM_ERR_INVALID_ARG;
   if (d->combine_mode != TLLM_COMBINE_KERNEL && d->combine_mode != TLLM_COMBINE_FUSED) return TLLM_ERR_INVALID_ARG;
+  if (d->test_stall != 0 && d->test_stall != 1) return TLLM_ERR_INVALID_ARG;
   return TLLM_OK;
 }
 
@@ -395,6 +396,7 @@ tllm_status make_params(const void* q, const void* k_cache, const void* v_cache,
   p->v_dim_major = d.v_layout == TLLM_V_DIM_MAJOR;
   p->rec_type = d.record_type;
   p->fused = pl.fused_combine != 0;
+  p->test_stall = d.test_stall;
   // alignment the chosen kernel's copies need (TMA boxes, 16-byte loads and stores)
   bool aligned = true;
   switch (pl.kernel) {

@@ -40,6 +40,7 @@ struct Params {
   int v_dim_major;                  // v_cache [num_pages, Hkv, D, bs] (TLLM_V_DIM_MAJOR)
   int rec_type;                     // tllm_record_type of the split records
   int fused;                        // the partial kernel merges the splits (no combine launch)
+  int test_stall;                   // failure-detection tests: the widening kernel issues no QK^T
 };
 
 // Element i of the split-record area: fp32, or bf16 / f16 when the plan asked for 16-bit records.

@@ -303,7 +303,8 @@ __global__ void __launch_bounds__(kThreads)
       if (warp == 1) {
         const uint32_t idqk = idesc_f16(128, kT, 0, 0, 0);   // Q and K in f16
         ok = mbar_wait(bars.q_full(), 0, abort);
-        for (int j = 0; ok && j < n_tiles; j++) {
+        // (a failure-detection test stalls here: no QK^T, so every wait on S runs out)
+        for (int j = 0; ok && j < n_tiles && !p.test_stall; j++) {
           const int sb = j & 1;                            // S buffer and f16 K buffer of tile j
           if (!mbar_wait(bars.fullK16(sb), (j >> 1) & 1, abort)) { ok = false; break; }
           if (j >= 2 && !mbar_wait(bars.s_free(sb), ((j >> 1) - 1) & 1, abort)) { ok = false; break; }

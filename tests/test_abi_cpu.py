@@ -157,6 +157,7 @@ def test_misaligned_workspace_is_rejected(lib):
     ("block_size", 512, B.TLLM_ERR_UNSUPPORTED),
     ("num_pages", 0, B.TLLM_ERR_INVALID_ARG),
     ("softmax_scale", -1.0, B.TLLM_ERR_INVALID_ARG),
+    ("test_stall", 2, B.TLLM_ERR_INVALID_ARG),
 ])
 def test_plan_rejects_bad_desc(lib, field, value, status):
     d = B.desc_for(W.single_decode())

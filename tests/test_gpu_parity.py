@@ -987,3 +987,33 @@ def test_simt_row_blocks_pinned(kv_dtype, D, Hq, Hkv, Lq):
         out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_SIMT, splits=S)
         assert plan.kernel == B.TLLM_KERNEL_SIMT
         assert_close(out, ref, wl.kv_dtype, f"simt pinned {kv_dtype} D{D} rows {Hq // Hkv * Lq} S{S}")
+
+
+# --- failure detection: a bounded wait that runs out ------------------------------------
+
+def test_pipeline_wait_timeout_is_reported_and_the_context_recovers():
+    """Failure detection without a GPU fault: with the test stall the widening kernel's QK^T
+    issuer issues nothing, so the waits on S run out after their 2 s bound. The kernel sets
+    TLLM_FLAG_TIMEOUT, skips its output stores (one split: the output keeps its NaN fill) and
+    frees its tensor memory; the next calls on the same context run normally and match the
+    oracle."""
+    import time
+    wl = W.verify16_int8().replace(ctx=[700, 300], extra_pages=2)
+    inp = _inputs(wl, 310)
+    ref, _ = oracle_out(inp)
+    for S in (1, 2):
+        desc = B.desc_for(wl, TCI8, num_pages=inp.num_pages)
+        desc.test_stall = 1
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        ws = B.Workspace(plan)
+        out = new_out(wl).fill_(float("nan"))
+        t = time.time()
+        B.run(inp, ws, out)
+        torch.cuda.synchronize()
+        assert time.time() - t < 60
+        assert B.tllm_decode_attn_read_status(ws, reset=True) & B.TLLM_FLAG_TIMEOUT
+        if S == 1:
+            assert torch.isnan(out.float()).all(), "a timed-out call stored output"
+        good, _, ws2 = run_gpu(inp, TCI8, splits=S)
+        assert not (B.tllm_decode_attn_read_status(ws2) & B.TLLM_FLAG_TIMEOUT)
+        assert_close(good, ref, wl.kv_dtype, f"after a timed-out call S{S}")
