@@ -1,13 +1,14 @@
-"""A model of the widening tensor-core kernel's mbarrier protocol, run under random schedules.
+"""Models of the tensor-core kernels' mbarrier protocols, run under random schedules.
 
-Each role of the kernel (the K and V producers, the converter warps, the two MMA issuers, the
-softmax warps) is a sequence of waits on, and arrivals at, the kernel's mbarriers in the order
-the CUDA source issues them; the asynchronous arrivals (TMA copies landing, tcgen05.commit)
+Each role of a kernel (producers, converter warps, MMA issuers, softmax warps) is a sequence of
+waits on, and arrivals at, the kernel's mbarriers in the order the CUDA source issues them; the asynchronous arrivals (TMA copies landing, tcgen05.commit)
 happen at random later moments. An mbarrier wait names a phase by its parity only, so the
 protocol is correct only if every wait for phase k starts when the barrier has completed k or
 k + 1 phases and no barrier completes phase k + 2 while a wait for phase k is still pending.
-The test checks that, and that every schedule runs to its end, for 1 to 12 tiles per item;
-and that the check catches a planted mistake.
+The tests check that, and that every schedule runs to its end, for 1 to 12 tiles per item, for
+the widening kernel and for the FP8 kernel (whose softmax warps are modelled one by one, two per
+warpgroup, so that a fast warp can run ahead of a slow one); and that the check catches a
+planted mistake.
 """
 import random
 
@@ -17,10 +18,14 @@ SK, SV = 2, 3          # staging ring depths: K, V
 
 
 class Bar:
-    def __init__(self, name):
-        self.name, self.done = name, 0
+    def __init__(self, name, count=1):
+        self.name, self.done, self.count, self.pending = name, 0, count, 0
 
-    def complete(self, waits):
+    def arrive(self, waits):
+        self.pending += 1
+        if self.pending < self.count:
+            return
+        self.pending = 0
         for (bar, k, who) in waits:
             if bar is self and k < self.done:
                 raise AssertionError(f"{self.name}: phase {self.done} completes while {who} still waits phase {k}")
@@ -95,16 +100,84 @@ def roles(n, rnd, rescale_p, skip_v_wait=False):
             "soft": soft()}
 
 
-def run(n, seed, rescale_p=0.3, skip_v_wait=False):
+SM_WARPS = 2          # softmax warps modelled per warpgroup (the kernel has 8)
+FP8_STAGES = 4
+FP8_COUNTS = {"sfree": SM_WARPS, "pfull": SM_WARPS, "xmax": SM_WARPS, "q": SM_WARPS, "fin": 2}
+
+
+def fp8_roles(n, rnd, partial_p, skip_p_wait=False):
+    """The FP8 kernel: K and V producers (4-stage rings, two tiles per step), the QK^T and PV
+    issuers, and two softmax warpgroups taking tiles wg, wg + 2, ... with their own S buffer,
+    P buffer and row-maximum barrier (split phase: arrive, work, wait)."""
+    def prod(name):
+        for j0 in range(0, n, 2):
+            for j in range(j0, min(n, j0 + 2)):
+                if j >= FP8_STAGES:
+                    yield ("wait", f"{name}empty{j % FP8_STAGES}", j // FP8_STAGES - 1)
+            for j in range(j0, min(n, j0 + 2)):
+                yield ("async", [f"{name}full{j % FP8_STAGES}"])
+        for j in range(max(0, n - FP8_STAGES), n):
+            yield ("wait", f"{name}full{j % FP8_STAGES}", j // FP8_STAGES)
+        for j in range(max(0, n - FP8_STAGES), n):
+            yield ("wait", f"{name}empty{j % FP8_STAGES}", j // FP8_STAGES)
+
+    def qk():
+        yield ("wait", "q", 0)
+        for j in range(n):
+            yield ("wait", f"kfull{j % FP8_STAGES}", j // FP8_STAGES)
+            if j >= 2:
+                yield ("wait", f"sfree{j & 1}", (j >> 1) - 1)
+            yield ("async", [f"sfull{j & 1}", f"kempty{j % FP8_STAGES}"])
+        yield ("async", ["fin"])
+        yield ("wait", "fin", 0)
+
+    def pv():
+        for j in range(n):
+            yield ("wait", f"pfull{j & 1}", j >> 1)
+            yield ("wait", f"vfull{j % FP8_STAGES}", j // FP8_STAGES)
+            yield ("async", [f"pv{j & 1}", f"vempty{j % FP8_STAGES}"])
+        yield ("async", ["fin"])
+        yield ("wait", "fin", 0)
+
+    def soft(wg, duty):
+        if wg == 0:
+            yield ("arrive", "q")
+        else:
+            yield ("wait", "q", 0)
+        last = -1
+        for j in range(wg, n, 2):
+            last = j
+            yield ("wait", f"sfull{wg}", j >> 1)
+            if duty and rnd.random() < partial_p:           # a partial tile: its V rows are zeroed
+                yield ("wait", f"vfull{j % FP8_STAGES}", j // FP8_STAGES)
+            yield ("arrive", f"sfree{wg}")
+            yield ("arrive", f"xmax{wg}")
+            yield ("wait", f"xmax{wg}", j >> 1)
+            if j >= 2 and not skip_p_wait:
+                yield ("wait", f"pv{wg}", (j - 2) >> 1)
+            yield ("arrive", f"pfull{wg}")
+        if last >= 0:
+            yield ("wait", f"pv{wg}", last >> 1)
+
+    actors = {"prodK": prod("k"), "prodV": prod("v"), "qk": qk(), "pv": pv()}
+    for wg in range(2):
+        for w in range(SM_WARPS):
+            actors[f"soft{wg}.{w}"] = soft(wg, duty=w == 0)
+    return actors
+
+
+def run(n, seed, rescale_p=0.3, skip_v_wait=False, model="widening", skip_p_wait=False):
     rnd = random.Random(seed)
     bars = {}
+    counts = FP8_COUNTS if model == "fp8" else {}
 
     def bar(name):
         if name not in bars:
-            bars[name] = Bar(name)
+            bars[name] = Bar(name, counts.get(name.rstrip("0123456789"), 1))
         return bars[name]
 
-    actors = roles(n, rnd, rescale_p, skip_v_wait)
+    actors = (roles(n, rnd, rescale_p, skip_v_wait) if model == "widening"
+              else fp8_roles(n, rnd, rescale_p, skip_p_wait))
     cur = {k: next(g, None) for k, g in actors.items()}
     pending = []
     for _ in range(200000):
@@ -116,13 +189,13 @@ def run(n, seed, rescale_p=0.3, skip_v_wait=False):
             return
         c = rnd.choice(choices)
         if c == "async":
-            bar(pending.pop(rnd.randrange(len(pending)))).complete(waits)
+            bar(pending.pop(rnd.randrange(len(pending)))).arrive(waits)
             continue
         a = cur[c]
         if a[0] == "wait":
             assert bar(a[1]).done <= a[2] + 1, f"{c} waits {a[1]} phase {a[2]} after {bar(a[1]).done} phases"
         elif a[0] == "arrive":
-            bar(a[1]).complete(waits)
+            bar(a[1]).arrive(waits)
         else:
             pending.extend(a[1])
         cur[c] = next(actors[c], None)
@@ -144,3 +217,18 @@ def test_the_protocol_check_catches_a_missing_wait():
     with pytest.raises(AssertionError):
         for seed in range(200):
             run(6, seed, skip_v_wait=True)
+
+
+@pytest.mark.parametrize("n", list(range(1, 13)))
+def test_fp8_kernel_barrier_protocol(n):
+    for seed in range(100):
+        run(n, 104729 * n + seed, model="fp8")
+
+
+def test_the_fp8_protocol_check_catches_a_missing_wait():
+    """Writing P without waiting for the PV that read the buffer two tiles before lets the P
+    buffer's barrier run ahead of the PV issuer."""
+    with pytest.raises(AssertionError):
+        for n in range(3, 9):
+            for seed in range(200):
+                run(n, seed, model="fp8", skip_p_wait=True)
