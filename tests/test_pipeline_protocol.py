@@ -6,9 +6,9 @@ happen at random later moments. An mbarrier wait names a phase by its parity onl
 protocol is correct only if every wait for phase k starts when the barrier has completed k or
 k + 1 phases and no barrier completes phase k + 2 while a wait for phase k is still pending.
 The tests check that, and that every schedule runs to its end, for 1 to 12 tiles per item, for
-the widening kernel and for the FP8 kernel (whose softmax warps are modelled one by one, two per
-warpgroup, so that a fast warp can run ahead of a slow one); and that the check catches a
-planted mistake.
+the widening kernel, the FP8 kernel and the 16-bit few-row kernel (softmax warps modelled one by
+one, so that a fast warp can run ahead of a slow one); and that the check catches planted
+mistakes.
 """
 import random
 
@@ -166,18 +166,77 @@ def fp8_roles(n, rnd, partial_p, skip_p_wait=False):
     return actors
 
 
+B16_STAGES = 3
+B16_COUNTS = {"sfree": SM_WARPS, "pfull": SM_WARPS, "q": SM_WARPS, "fin": 2}
+
+
+def b16_roles(n, rnd, p_rare):
+    """The 16-bit few-row kernel: K and V producers (3-stage rings), the S^T and O^T issuers,
+    and one softmax group of warps taking every tile (two S and two P buffers)."""
+    def prod(name):
+        for j in range(n):
+            if j >= B16_STAGES:
+                yield ("wait", f"{name}empty{j % B16_STAGES}", j // B16_STAGES - 1)
+            yield ("async", [f"{name}full{j % B16_STAGES}"])
+        for j in range(max(0, n - B16_STAGES), n):
+            yield ("wait", f"{name}full{j % B16_STAGES}", j // B16_STAGES)
+        for j in range(max(0, n - B16_STAGES), n):
+            yield ("wait", f"{name}empty{j % B16_STAGES}", j // B16_STAGES)
+
+    def qk():
+        yield ("wait", "q", 0)
+        for j in range(n):
+            yield ("wait", f"kfull{j % B16_STAGES}", j // B16_STAGES)
+            if j >= 2:
+                yield ("wait", f"sfree{j & 1}", (j >> 1) - 1)
+            yield ("async", [f"sfull{j & 1}", f"kempty{j % B16_STAGES}"])
+        yield ("async", ["fin"])
+        yield ("wait", "fin", 0)
+
+    def pv():
+        for j in range(n):
+            yield ("wait", f"pfull{j & 1}", j >> 1)
+            yield ("wait", f"vfull{j % B16_STAGES}", j // B16_STAGES)
+            yield ("async", [f"pv{j & 1}", f"vempty{j % B16_STAGES}"])
+        yield ("async", ["fin"])
+        yield ("wait", "fin", 0)
+
+    def soft():
+        yield ("arrive", "q")
+        for j in range(n):
+            yield ("wait", f"sfull{j & 1}", j >> 1)
+            if rnd.random() < p_rare:                      # a token not read: its V rows are zeroed
+                yield ("wait", f"vfull{j % B16_STAGES}", j // B16_STAGES)
+            yield ("arrive", f"sfree{j & 1}")
+            if j >= 2:
+                yield ("wait", f"pv{j & 1}", (j - 2) >> 1)
+            if j >= 1 and rnd.random() < p_rare:          # the reference moved: O is rescaled
+                yield ("wait", f"pv{(j - 1) & 1}", (j - 1) >> 1)
+            yield ("arrive", f"pfull{j & 1}")
+        yield ("wait", f"pv{(n - 1) & 1}", (n - 1) >> 1)
+
+    actors = {"prodK": prod("k"), "prodV": prod("v"), "qk": qk(), "pv": pv()}
+    for w in range(SM_WARPS):
+        actors[f"soft{w}"] = soft()
+    return actors
+
+
 def run(n, seed, rescale_p=0.3, skip_v_wait=False, model="widening", skip_p_wait=False):
     rnd = random.Random(seed)
     bars = {}
-    counts = FP8_COUNTS if model == "fp8" else {}
+    counts = {"fp8": FP8_COUNTS, "b16": B16_COUNTS}.get(model, {})
 
     def bar(name):
         if name not in bars:
             bars[name] = Bar(name, counts.get(name.rstrip("0123456789"), 1))
         return bars[name]
 
-    actors = (roles(n, rnd, rescale_p, skip_v_wait) if model == "widening"
-              else fp8_roles(n, rnd, rescale_p, skip_p_wait))
+    if model == "widening":
+        actors = roles(n, rnd, rescale_p, skip_v_wait)
+    elif model == "fp8":
+        actors = fp8_roles(n, rnd, rescale_p, skip_p_wait)
+    else:
+        actors = b16_roles(n, rnd, rescale_p)
     cur = {k: next(g, None) for k, g in actors.items()}
     pending = []
     for _ in range(200000):
@@ -232,3 +291,9 @@ def test_the_fp8_protocol_check_catches_a_missing_wait():
         for n in range(3, 9):
             for seed in range(200):
                 run(n, seed, model="fp8", skip_p_wait=True)
+
+
+@pytest.mark.parametrize("n", list(range(1, 13)))
+def test_sixteen_bit_kernel_barrier_protocol(n):
+    for seed in range(100):
+        run(n, 15485863 * n + seed, model="b16")
