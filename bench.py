@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--bs", type=int, default=0, help="override the block size (profiling)")
     ap.add_argument("--splits", type=int, default=0, help="override the planner's split count (0: plan it)")
     ap.add_argument("--record", default="f32", choices=["f32", "bf16", "f16"], help="split-record element type")
+    ap.add_argument("--v-layout", default="token_major", choices=["token_major", "dim_major"],
+                    help="V cache layout of the timed workload (dim_major: [pages, Hkv, D, bs])")
     ap.add_argument("--no-other-configs", action="store_true", help="time only the headline workload")
     ap.add_argument("--other-steps", type=int, default=50, help="timed replays of each other workload")
     return ap.parse_args()
@@ -294,13 +296,17 @@ class Measured:
     served from L2 on the next step: then every timed replay is preceded (outside its events)
     by a write of a buffer twice the L2 size."""
 
-    def __init__(self, wl, seed, dev, stream, kernel, splits=0, record="f32"):
+    def __init__(self, wl, seed, dev, stream, kernel, splits=0, record="f32", v_dim_major=False):
         from split_kv_paged_gb300 import binding as B
         self.B = B
         self.wl, self.dev, self.stream = wl, dev, stream
         self.inp = W.make_inputs(wl, seed, device=dev)
+        if v_dim_major:
+            # the same V values, stored [pages, Hkv, D, bs]
+            self.inp.v_cache = self.inp.v_cache.transpose(-1, -2).contiguous()
         rec = {"f32": B.TLLM_RECORD_F32, "bf16": B.TLLM_RECORD_BF16, "f16": B.TLLM_RECORD_F16}[record]
-        desc = B.desc_for(wl, kernel, num_pages=self.inp.num_pages, record_type=rec)
+        vl = B.TLLM_V_DIM_MAJOR if v_dim_major else B.TLLM_V_TOKEN_MAJOR
+        desc = B.desc_for(wl, kernel, num_pages=self.inp.num_pages, record_type=rec, v_layout=vl)
         n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
         plan_args = (desc, wl.B, wl.Lq, wl.window)
         plan_kw = dict(host_ctx_lens=wl.ctx, num_sms=n_sm, splits_override=splits)
@@ -472,7 +478,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     wl = workload(args)
     stream = torch.cuda.Stream(device=dev)
-    m = Measured(wl, rank_seed(rank), dev, stream, kernel_code(args.kernel), args.splits, args.record)
+    m = Measured(wl, rank_seed(rank), dev, stream, kernel_code(args.kernel), args.splits, args.record,
+                 args.v_layout == "dim_major")
     plan, inp, out, S, nbytes = m.plan, m.inp, m.out, m.S, m.nbytes
 
     def barrier():
@@ -550,7 +557,8 @@ def main():
     # its power cap, which would slow the short latency-bound workloads measured after them
     options = {}
     if rank == 0 and world == 1 and not args.no_other_configs and args.workload == "mtp4_fp8_long" \
-            and args.batch == 0 and args.ctx == 0 and args.bs == 0 and args.record == "f32" and args.kernel == "auto":
+            and args.batch == 0 and args.ctx == 0 and args.bs == 0 and args.record == "f32" and args.kernel == "auto" \
+            and args.v_layout == "token_major":
         for name, record, vdm in (("record_bf16", "bf16", False), ("v_dim_major", "f32", True)):
             options[name] = option_config(m, record, vdm, args.steps, max(3, min(args.warmup, 5)), peak)
 
@@ -564,7 +572,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": wl.name, "batch": wl.B, "ctx": max(wl.ctx), "query_rows": wl.Lq, "Hq": wl.Hq,
                    "Hkv": wl.Hkv, "head_dim": wl.D, "block_size": wl.bs, "num_splits": S,
-                   "kernel": int(plan.kernel), "record": args.record, "logical_bytes": nbytes, "plan_host_us": m.plan_us,
+                   "kernel": int(plan.kernel), "record": args.record, "v_layout": args.v_layout, "logical_bytes": nbytes, "plan_host_us": m.plan_us,
                    "l2": m.l2_note, "aggregation": "mean of the K timed graph replays",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

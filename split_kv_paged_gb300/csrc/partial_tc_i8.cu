@@ -144,8 +144,9 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// kKv: the cache's element type (kKvI8, kKvE4m3, kKvF16 or kKvBf16)
-template <int D, int kKv>
+// kKv: the cache's element type (kKvI8, kKvE4m3, kKvF16 or kKvBf16); kVdm: the V cache is
+// dimension-major ([pages, Hkv, D, bs]; a separate instance)
+template <int D, int kKv, bool kVdm>
 __global__ void __launch_bounds__(kThreads)
     partial_tc_i8_kernel(const Params p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
@@ -271,8 +272,15 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) mbar_arrive_expect_tx(full(st), __popc(mask) * (uint32_t)brows * D * kEsz);
       __syncwarp();
       if (pg >= 0) {
-        const int row = (int)(((int64_t)pg * p.Hkv + g) * bs + (bs > kT ? (tt & (bs - 1)) : 0));
-        tma_load_2d(stg + lane * brows * D * kEsz, isk ? &kmap : &vmap, 0, row, full(st));
+        if (isk || !kVdm) {
+          const int row = (int)(((int64_t)pg * p.Hkv + g) * bs + (bs > kT ? (tt & (bs - 1)) : 0));
+          tma_load_2d(stg + lane * brows * D * kEsz, isk ? &kmap : &vmap, 0, row, full(st));
+        } else {
+          // a dimension-major V page: one box of D rows (dims) x brows tokens, staged as
+          // [D][brows] behind the page slots before it
+          tma_load_2d(stg + lane * brows * D * kEsz, &vmap, bs > kT ? (tt & (bs - 1)) : 0,
+                      (int)(((int64_t)pg * p.Hkv + g) * D), full(st));
+        }
       }
       // scales (quantised caches): lanes 0..15 copy the scales of tokens 4l..4l+3; every lane
       // arrives once its copy (if any) has landed
@@ -318,7 +326,9 @@ __global__ void __launch_bounds__(kThreads)
           mma_commit(bars.emptyK16(sb));
         }
       } else {
-        const uint32_t idpv = idesc_f16(128, D, kPParts - 1, 0, 1);   // P and V in f16 (bf16 V: both bf16)
+        // P and V in f16 (bf16 V: both bf16); V MN-major as widened from token-major pages, K-major
+        // (8-token blocks of D rows x 16 bytes) from dimension-major ones
+        const uint32_t idpv = idesc_f16(128, D, kPParts - 1, 0, kVdm ? 0 : 1);
         const uint32_t vt = sbase + S::kOff16 + 2 * S::kHalf16;
         for (int j = 0; ok && j < n_tiles; j++) {
           const int pb = j & 1;
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(kThreads)
             for (int part = 0; part < kPParts; part++)
               mma_f16_ss(tmem + kColO,
                          sdesc_sw128(sbase + S::kOffP + pb * S::kPBuf + part * S::kPPart + 32 * k, 16, 1024),
-                         sdesc_sw128(vt + 2048 * k, S::kAtom, 1024), idpv, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
+                         kVdm ? sdesc_none(vt + 32 * D * k, 16 * D, 128) : sdesc_sw128(vt + 2048 * k, S::kAtom, 1024),
+                         idpv, (j > 0 || k > 0 || part > 0) ? 1u : 0u);
           mma_commit(bars.pv_done(pb));
           mma_commit(bars.emptyV16());
         }
@@ -381,7 +392,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
           const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
-          w[i] = *reinterpret_cast<const uint4*>(src + (t * D + d0) * kEsz);
+          // (a dimension-major V stage holds the same bytes in the order page slot, dim, token:
+          // chunk c is the c-th 16 bytes of it)
+          w[i] = *reinterpret_cast<const uint4*>(src + (kVdm && which == 1 ? 16 * c : (t * D + d0) * kEsz));
         }
         // A bf16 K tile enters f16 scaled by 2^e, e from the largest |x| the split reads in it,
         // so that this maximum lies in [2^13, 2^14): every element within 2^-27 of it converts to
@@ -439,6 +452,47 @@ __global__ void __launch_bounds__(kThreads)
         const uint32_t dst = sbase + S::kOff16 + (which == 0 ? (j & 1) : 2) * S::kHalf16;
         const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
         const float emul = __int_as_float((e + 127) << 23);
+        if (kVdm && which == 1) {
+          // dimension-major V: chunk c holds kEpc tokens of one dim of one page slot; widened,
+          // they go to the K-major f16 V buffer, whose 8-token blocks are D rows x 16 bytes.
+          // Tokens the split does not read are zeroed element by element (e4m3 and 16-bit codes
+          // may be NaN there; int8 is always finite).
+          const int cpr = brows * kEsz / 16;               // chunks per dim row of a page slot
+#pragma unroll
+          for (int i = 0; i < kPer; i++) {
+            const int c = ct + 128 * i, slot = c / (D * cpr), rem = c % (D * cpr), d = rem / cpr;
+            const int t0c = slot * brows + (rem % cpr) * kEpc;      // first token of the chunk
+            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            uint32_t h[8];
+            if constexpr (!k16) {
+              if constexpr (kKv == kKvE4m3) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) h[q] = e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1))));
+              } else {
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                  const uint32_t x = __byte_perm(ws[q >> 1] ^ 0x80808080u, 0x64646464u, (q & 1) ? 0x5342u : 0x5140u);
+                  const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+                  h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; q++) h[q] = ws[q];
+            }
+            if constexpr (kKv != kKvI8) {
+#pragma unroll
+              for (int q = 0; q < kEpc / 2; q++)
+                h[q] &= (read_tok(t0c + 2 * q) ? 0x0000ffffu : 0u) | (read_tok(t0c + 2 * q + 1) ? 0xffff0000u : 0u);
+            }
+            const uint32_t a0 = dst + (t0c >> 3) * (16 * D) + 16 * d;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                         "r"(h[3]));
+            if constexpr (!k16)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 16 * D), "r"(h[4]), "r"(h[5]),
+                           "r"(h[6]), "r"(h[7]));
+          }
+        } else {
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
           const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
@@ -484,6 +538,7 @@ __global__ void __launch_bounds__(kThreads)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]), "r"(h[1]),
                          "r"(h[2]), "r"(h[3]));
           }
+        }
         }
         fence_proxy_async();
         __syncwarp();
@@ -849,14 +904,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder_i8() {
   return fn;
 }
 
-// 2-D map over the cache viewed as [pages * Hkv * bs rows][D elements of esz bytes]; a box is
-// one page (or one 64-token tile of a larger page), unswizzled: the converters read it row by row.
-bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int D, int box_rows, int esz) {
+// 2-D map over the cache viewed as [rows][inner elements of esz bytes], unswizzled (the
+// converters read it row by row). Token-major: rows = pages * Hkv * bs, inner = D, a box one page
+// (or one 64-token tile of a larger page). Dimension-major V: rows = pages * Hkv * D, inner = bs,
+// a box D rows x box_inner tokens.
+bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int inner, int box_rows, int esz,
+                   int box_inner = 0) {
   auto enc = get_encoder_i8();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * esz};
-  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(box_inner ? box_inner : inner), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
              const_cast<void*>(base), dims, strides, box, estr,
@@ -864,37 +922,45 @@ bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int D, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int kKv>
+template <int D, int kKv, bool kVdm>
 cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   constexpr int kEsz = (kKv == kKvF16 || kKv == kKvBf16) ? 2 : 1;
   using S = Lay<D, kEsz, kKv == kKvBf16 ? 2 : 1>;
   CUtensorMap km, vm;
   const int64_t rows = (int64_t)p.num_pages * p.Hkv * p.bs;
   const int box_rows = p.bs < kT ? p.bs : kT;
-  if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows, kEsz) || !encode_i8_map(&vm, p.v_cache, rows, D, box_rows, kEsz))
+  if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows, kEsz)) return cudaErrorInvalidValue;
+  // dimension-major V: [pages * Hkv * D rows][bs tokens], a box of box_rows tokens x D rows
+  if (kVdm ? !encode_i8_map(&vm, p.v_cache, (int64_t)p.num_pages * p.Hkv * D, p.bs, D, kEsz, box_rows)
+           : !encode_i8_map(&vm, p.v_cache, rows, D, box_rows, kEsz))
     return cudaErrorInvalidValue;
   constexpr int smem = (int)S::kSmem;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kKv>), smem);
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kKv, kVdm>), smem);
   if (e != cudaSuccess) return e;
   const int n_items = p.B * p.Hkv * p.num_splits;
   const int n_sm = sm_count();
   if (n_sm <= 0) return cudaErrorInvalidValue;
   dim3 grid(n_items < n_sm ? n_items : n_sm);
-  partial_tc_i8_kernel<D, kKv><<<grid, kThreads, smem, stream>>>(p, km, vm);
+  partial_tc_i8_kernel<D, kKv, kVdm><<<grid, kThreads, smem, stream>>>(p, km, vm);
   return cudaGetLastError();
+}
+
+template <int kKv, bool kVdm>
+cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
+  switch (p.D) {
+    case 64: return launch_d<64, kKv, kVdm>(p, stream);
+    case 128: return launch_d<128, kKv, kVdm>(p, stream);
+    case 256:
+      // a 16-bit tile of head_dim 256 would not leave room for the staging rings and f16 buffers
+      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv, kVdm>(p, stream);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int kKv>
 cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
-  switch (p.D) {
-    case 64: return launch_d<64, kKv>(p, stream);
-    case 128: return launch_d<128, kKv>(p, stream);
-    case 256:
-      // a 16-bit tile of head_dim 256 would not leave room for three staged tiles
-      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv>(p, stream);
-      return cudaErrorInvalidValue;
-    default: return cudaErrorInvalidValue;
-  }
+  return p.v_dim_major ? launch_kv<kKv, true>(p, stream) : launch_kv<kKv, false>(p, stream);
 }
 
 }  // namespace
@@ -903,10 +969,13 @@ bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   const bool quant = d.kv_dtype == TLLM_INT8 || d.kv_dtype == TLLM_FP8_E4M3;
   const bool b16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
+  // a transposed V cache: a page's dimension row must be a whole number of 16-byte chunks
+  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || (d.v_layout == TLLM_V_DIM_MAJOR && (b16 || bs >= 16));
   return (quant || b16) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
-         (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && quant)) && d.v_layout == TLLM_V_TOKEN_MAJOR &&
+         (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && quant)) && v_ok &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
-         (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31);
+         (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31) &&
+         (int64_t)d.num_pages * d.num_kv_heads * d.head_dim < ((int64_t)1 << 31);   // (a transposed V's rows)
 }
 
 bool tc_i8_pointers_ok(const Params& p) {

@@ -306,9 +306,10 @@ def test_contiguous_cache_needs_every_request_block(lib):
 
 def test_dim_major_v_routes_to_kernels_that_read_it(lib):
     """AUTO with a transposed V cache: the FP8 tensor-core kernel for FP8 KV (head_dim 128, pages
-    of 16 or more tokens, at most 64 rows); the pipelined CUDA-core kernel (in row blocks past 8
-    rows) for the other shapes, except 8-bit caches with 8-token pages, which the generic kernel
-    reads."""
+    of 16 or more tokens, at most 64 rows); the widening tensor-core kernel for more than 8 rows
+    of the other quantised shapes (pages of 16 or more tokens) and of 16-bit caches up to
+    head_dim 128; the pipelined CUDA-core kernel for the rest, except 8-bit caches with 8-token
+    pages, which the generic kernel reads."""
     def plan(wl):
         return B.tllm_decode_attn_plan(B.desc_for(wl, v_layout=B.TLLM_V_DIM_MAJOR), wl.B, wl.Lq, 0,
                                        host_ctx_lens=wl.ctx)
@@ -316,8 +317,10 @@ def test_dim_major_v_routes_to_kernels_that_read_it(lib):
     assert plan(W.mtp4_fp8_long(batch=2, ctx=4000, bs=8)).kernel == B.TLLM_KERNEL_GENERIC
     assert plan(W.window_sink_bf16(batch=2)).kernel == B.TLLM_KERNEL_SIMT
     assert plan(W.window_sink_bf16(batch=2).replace(bs=8, D=256, Hq=32, Hkv=2)).kernel == B.TLLM_KERNEL_SIMT
-    assert plan(W.verify16_int8()).kernel == B.TLLM_KERNEL_SIMT
-    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000).replace(D=64)).kernel == B.TLLM_KERNEL_SIMT
+    assert plan(W.verify16_int8()).kernel == B.TLLM_KERNEL_TC_I8
+    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000).replace(D=64)).kernel == B.TLLM_KERNEL_TC_I8
+    assert plan(W.window_sink_bf16(batch=2).replace(bs=8, D=128, Hq=32, Hkv=2)).kernel == B.TLLM_KERNEL_TC_I8
+    assert plan(W.verify16_int8().replace(Lq=1)).kernel == B.TLLM_KERNEL_SIMT        # 6 rows
     assert plan(W.verify16_int8().replace(bs=8)).kernel == B.TLLM_KERNEL_GENERIC
 
 

@@ -771,10 +771,10 @@ def test_dim_major_v_cache(bs, kernel):
     ("f16", "bf16", 128, 16, 12, 4, 3),
 ])
 def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
-    """The pipelined CUDA-core kernel on a transposed V cache (AUTO's choice for every shape the
-    FP8 tensor-core kernel does not take): every cache type and head_dim, pages of 8 to 128
-    tokens, one row block and several, with a window, sinks, ragged lengths and poisoned tails
-    and pages."""
+    """The pipelined CUDA-core kernel on a transposed V cache (AUTO's choice for 8 rows or fewer
+    where the FP8 tensor-core kernel does not apply, pinned here for more): every cache type and
+    head_dim, pages of 8 to 128 tokens, one row block and several, with a window, sinks, ragged
+    lengths and poisoned tails and pages."""
     wl = W.verify16_int8().replace(ctx=[3000, 700, 65, 9], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, bs=bs, kv_dtype=kv_dtype,
                                    q_dtype=q_dtype, window=900, sinks=True, extra_pages=4,
                                    kv_std=0.5 if kv_dtype == "e4m3" else 1.0)
@@ -782,7 +782,7 @@ def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
     ref, _ = oracle_out(inp)
     v_dm = inp.v_cache.transpose(-1, -2).contiguous()
     for S in (1, 3):
-        desc = B.desc_for(wl, B.TLLM_KERNEL_AUTO, num_pages=inp.num_pages, v_layout=B.TLLM_V_DIM_MAJOR)
+        desc = B.desc_for(wl, B.TLLM_KERNEL_SIMT, num_pages=inp.num_pages, v_layout=B.TLLM_V_DIM_MAJOR)
         plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
         assert plan.kernel == B.TLLM_KERNEL_SIMT
         ws = poisoned_workspace(plan)
@@ -792,6 +792,37 @@ def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
         torch.cuda.synchronize()
         assert not (B.tllm_decode_attn_read_status(ws) & B.TLLM_FLAG_TIMEOUT)
         assert_close(out, ref, wl.kv_dtype, f"dim-major V simt {kv_dtype} D{D} bs{bs} S{S}")
+
+
+@pytest.mark.parametrize("kv_dtype,q_dtype,D,bs,Hq,Hkv,Lq", [
+    ("i8", "bf16", 256, 16, 24, 4, 16), ("e4m3", "bf16", 64, 64, 16, 1, 4), ("i8", "f16", 128, 128, 8, 2, 4),
+    ("f16", "f16", 64, 8, 14, 2, 2), ("bf16", "bf16", 128, 16, 32, 8, 4), ("bf16", "bf16", 64, 32, 32, 2, 2),
+    ("f16", "f16", 128, 128, 12, 4, 3), ("e4m3", "f16", 128, 32, 16, 2, 8), ("i8", "bf16", 64, 16, 16, 1, 8),
+    ("e4m3", "bf16", 256, 16, 8, 1, 1),
+])
+def test_dim_major_v_widening_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
+    """The widening tensor-core kernel on a transposed V cache (AUTO's choice past 8 rows where
+    the FP8 kernel does not apply): each page's [D, bs] block is staged as it lies and widened
+    into the K-major f16 operand of the PV product. Every cache type, head_dim 64 to 256, pages
+    of 8 to 128 tokens, 8 to 128 rows, with a window, sinks, ragged lengths and poisoned tails
+    and pages (whose NaN codes must not reach the product)."""
+    wl = W.verify16_int8().replace(ctx=[3000, 700, 65, 9], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, bs=bs, kv_dtype=kv_dtype,
+                                   q_dtype=q_dtype, window=900, sinks=True, extra_pages=4,
+                                   kv_std=0.5 if kv_dtype == "e4m3" else 1.0)
+    inp = _inputs(wl, 400 + D + bs + Hq)
+    ref, _ = oracle_out(inp)
+    v_dm = inp.v_cache.transpose(-1, -2).contiguous()
+    for S in (1, 3):
+        desc = B.desc_for(wl, B.TLLM_KERNEL_TC_I8, num_pages=inp.num_pages, v_layout=B.TLLM_V_DIM_MAJOR)
+        plan = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=S)
+        assert plan.kernel == B.TLLM_KERNEL_TC_I8
+        ws = poisoned_workspace(plan)
+        out = new_out(wl)
+        B.tllm_decode_attn_splitkv(inp.q, inp.k_cache, v_dm, inp.block_table, inp.context_lens, wl.Lq,
+                                   inp.kv_scales, inp.sinks, wl.window, S, ws, out)
+        torch.cuda.synchronize()
+        assert not (B.tllm_decode_attn_read_status(ws) & B.TLLM_FLAG_TIMEOUT)
+        assert_close(out, ref, wl.kv_dtype, f"dim-major V widening {kv_dtype} D{D} bs{bs} S{S}")
 
 
 # --- 16-bit split records -------------------------------------------------------------
