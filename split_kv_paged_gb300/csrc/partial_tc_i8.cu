@@ -457,11 +457,13 @@ __global__ void __launch_bounds__(kThreads)
           // they go to the K-major f16 V buffer, whose 8-token blocks are D rows x 16 bytes.
           // Tokens the split does not read are zeroed element by element (e4m3 and 16-bit codes
           // may be NaN there; int8 is always finite).
-          const int cpr = brows * kEsz / 16;               // chunks per dim row of a page slot
+          // (all powers of two: a page slot's dim row is 2^csh chunks, a slot D << csh chunks)
+          constexpr int kDsh = D == 64 ? 6 : D == 128 ? 7 : 8, kEsh = kEsz == 2 ? 3 : 4;
+          const int bsh = bs_sh < 6 ? bs_sh : 6, csh = bsh - kEsh;
 #pragma unroll
           for (int i = 0; i < kPer; i++) {
-            const int c = ct + 128 * i, slot = c / (D * cpr), rem = c % (D * cpr), d = rem / cpr;
-            const int t0c = slot * brows + (rem % cpr) * kEpc;      // first token of the chunk
+            const int c = ct + 128 * i, rem = c & ((D << csh) - 1), d = rem >> csh;
+            const int t0c = ((c >> (kDsh + csh)) << bsh) + ((rem & ((1 << csh) - 1)) << kEsh);   // first token
             const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
             uint32_t h[8];
             if constexpr (!k16) {
