@@ -48,6 +48,11 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"((uint64_t)src), "r"(ok ? 16u : 0u)
                : "memory");
 }
+// 8-byte variant (through L1: the .cg form copies 16 bytes only)
+__device__ __forceinline__ void cp_async8_zfill(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"((uint64_t)src), "r"(ok ? 8u : 0u)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -302,14 +307,21 @@ __global__ void __launch_bounds__(kThreads, RM <= 4 ? 2 : 1) partial_simt_kernel
         cp_async16_zfill(vdst + tok * S::kRowStride + off, vc + row * S::kRowBytes + off, ok);
       } else {
         // dimension-major V: chunk c is 16 bytes of dim d's page row, tokens tl .. tl + 16 / kElt
-        // - 1 of the tile (on one page: bs is a multiple of 16 / kElt); a chunk any of whose
-        // tokens the split reads is copied whole, the rest zero-filled
+        // - 1 of the tile (on one page when bs is a multiple of 16 / kElt; else, 8-token pages of
+        // an 8-bit cache, its two 8-byte halves come from two pages); a piece any of whose tokens
+        // the split reads is copied whole, the rest zero-filled
         constexpr int kTpc = 16 / S::kElt;
-        const int d = c / S::kDmChunks, cc = c % S::kDmChunks, tl = cc * kTpc, tv = tt + tl;
-        const int pgv = pg_s[(jt % kPgSlots) * 32 + (tl >> bs_sh)];
-        const bool okv = jt < n_tiles && pgv >= 0 && tv + kTpc > vlo && tv < t1;
-        const int64_t src = okv ? ((((int64_t)pgv * p.Hkv + g) * D + d) * bs + (tv & (bs - 1))) * S::kElt : 0;
-        cp_async16_zfill(vdst + d * S::kDmRow + ((cc ^ ((d >> 3) & (S::kDmChunks - 1))) << 4), vc + src, okv);
+        const int d = c / S::kDmChunks, cc = c % S::kDmChunks, tl = cc * kTpc;
+        const uint32_t vd = vdst + d * S::kDmRow + ((cc ^ ((d >> 3) & (S::kDmChunks - 1))) << 4);
+        const int np = bs < kTpc ? 2 : 1, tpp = kTpc / np;     // pieces of the chunk, tokens each
+        for (int h = 0; h < np; h++) {
+          const int tlh = tl + h * tpp, tv = tt + tlh;
+          const int pgv = pg_s[(jt % kPgSlots) * 32 + (tlh >> bs_sh)];
+          const bool okv = jt < n_tiles && pgv >= 0 && tv + tpp > vlo && tv < t1;
+          const int64_t src = okv ? ((((int64_t)pgv * p.Hkv + g) * D + d) * bs + (tv & (bs - 1))) * S::kElt : 0;
+          if (np == 1) cp_async16_zfill(vd, vc + src, okv);
+          else cp_async8_zfill(vd + 8 * h, vc + src, okv);
+        }
       }
     }
     if constexpr (S::kScaled) {
@@ -551,10 +563,7 @@ bool simt_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   const bool kv_ok = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16 || d.kv_dtype == TLLM_FP8_E4M3 ||
                      d.kv_dtype == TLLM_INT8;
-  // a transposed V cache: a 16-byte copy must hold tokens of one page (16-bit: bs >= 8; 8-bit:
-  // bs >= 16)
-  const bool kv16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
-  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || (d.v_layout == TLLM_V_DIM_MAJOR && (kv16 || bs >= 16));
+  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || d.v_layout == TLLM_V_DIM_MAJOR;
   return kv_ok && v_ok && (d.head_dim == 64 || d.head_dim == 128 || d.head_dim == 256) &&
          rows >= 1 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128);
 }

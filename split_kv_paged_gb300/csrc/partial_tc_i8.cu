@@ -45,6 +45,7 @@
 //
 // Every wait is bounded in time; a timeout sets TLLM_FLAG_TIMEOUT, lets every role run to its
 // end without waiting, skips the output stores, takes no further item and frees TMEM.
+#include <cstring>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -144,13 +145,17 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// kKv: the cache's element type (kKvI8, kKvE4m3, kKvF16 or kKvBf16); kVdm: the V cache is
-// dimension-major ([pages, Hkv, D, bs]; a separate instance)
-template <int D, int kKv, bool kVdm>
+// V layouts, each a separate instance: token-major, dimension-major ([pages, Hkv, D, bs]), and
+// dimension-major with 8-byte dim rows (8-token pages of an 8-bit cache)
+constexpr int kVTok = 0, kVDim = 1, kVDim8 = 2;
+
+// kKv: the cache's element type (kKvI8, kKvE4m3, kKvF16 or kKvBf16); kVL: the V layout
+template <int D, int kKv, int kVL>
 __global__ void __launch_bounds__(kThreads)
     partial_tc_i8_kernel(const Params p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
   constexpr bool k16 = kKv == kKvF16 || kKv == kKvBf16;   // 16-bit cache: no per-token scales
+  constexpr bool kVdm = kVL != kVTok;
   constexpr int kEsz = k16 ? 2 : 1;
   constexpr int kPParts = kKv == kKvBf16 ? 2 : 1;          // bf16 V: P as high + low bf16 parts
   using S = Lay<D, kEsz, kPParts>;
@@ -275,11 +280,17 @@ __global__ void __launch_bounds__(kThreads)
         if (isk || !kVdm) {
           const int row = (int)(((int64_t)pg * p.Hkv + g) * bs + (bs > kT ? (tt & (bs - 1)) : 0));
           tma_load_2d(stg + lane * brows * D * kEsz, isk ? &kmap : &vmap, 0, row, full(st));
-        } else {
+        } else if (kVL == kVDim) {
           // a dimension-major V page: one box of D rows (dims) x brows tokens, staged as
           // [D][brows] behind the page slots before it
           tma_load_2d(stg + lane * brows * D * kEsz, &vmap, bs > kT ? (tt & (bs - 1)) : 0,
                       (int)(((int64_t)pg * p.Hkv + g) * D), full(st));
+        } else {
+          // 8-token pages of an 8-bit cache (8-byte dim rows, narrower than a box may be): the
+          // page's D x 8 contiguous bytes in one plain bulk copy
+          bulk_load(stg + lane * brows * D * kEsz,
+                    static_cast<const uint8_t*>(p.v_cache) + ((int64_t)pg * p.Hkv + g) * D * bs * kEsz,
+                    (uint32_t)(brows * D * kEsz), full(st));
         }
       }
       // scales (quantised caches): lanes 0..15 copy the scales of tokens 4l..4l+3; every lane
@@ -457,19 +468,22 @@ __global__ void __launch_bounds__(kThreads)
           // they go to the K-major f16 V buffer, whose 8-token blocks are D rows x 16 bytes.
           // Tokens the split does not read are zeroed element by element (e4m3 and 16-bit codes
           // may be NaN there; int8 is always finite).
-          // (all powers of two: a page slot's dim row is 2^csh chunks, a slot D << csh chunks)
-          constexpr int kDsh = D == 64 ? 6 : D == 128 ? 7 : 8, kEsh = kEsz == 2 ? 3 : 4;
-          const int bsh = bs_sh < 6 ? bs_sh : 6, csh = bsh - kEsh;
+          if constexpr (kVL == kVDim8) {
+            // 8-token pages of an 8-bit cache: chunk c holds the 8-token rows of dims d and
+            // d + 1 of page slot c / (D / 2); their widened rows are adjacent in the V buffer
+            constexpr int kDsh = D == 64 ? 6 : D == 128 ? 7 : 8;
 #pragma unroll
-          for (int i = 0; i < kPer; i++) {
-            const int c = ct + 128 * i, rem = c & ((D << csh) - 1), d = rem >> csh;
-            const int t0c = ((c >> (kDsh + csh)) << bsh) + ((rem & ((1 << csh) - 1)) << kEsh);   // first token
-            const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-            uint32_t h[8];
-            if constexpr (!k16) {
+            for (int i = 0; i < kPer; i++) {
+              const int c = ct + 128 * i, d = (c & (D / 2 - 1)) * 2, t0c = (c >> (kDsh - 1)) << 3;
+              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+              uint32_t h[8];
               if constexpr (kKv == kKvE4m3) {
 #pragma unroll
-                for (int q = 0; q < 8; q++) h[q] = e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1))));
+                for (int q = 0; q < 8; q++) {
+                  h[q] = e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1))));
+                  const int tq = t0c + 2 * (q & 3);
+                  h[q] &= (read_tok(tq) ? 0x0000ffffu : 0u) | (read_tok(tq + 1) ? 0xffff0000u : 0u);
+                }
               } else {
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
@@ -478,21 +492,50 @@ __global__ void __launch_bounds__(kThreads)
                   h[q] = *reinterpret_cast<const uint32_t*>(&v2);
                 }
               }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; q++) h[q] = ws[q];
+              const uint32_t a0 = dst + (t0c >> 3) * (16 * D) + 16 * d;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                           "r"(h[3]));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 16), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+                           "r"(h[7]));
             }
-            if constexpr (kKv != kKvI8) {
+          } else {
+            // (all powers of two: a page slot's dim row is 2^csh chunks, a slot D << csh chunks)
+            constexpr int kDsh = D == 64 ? 6 : D == 128 ? 7 : 8, kEsh = kEsz == 2 ? 3 : 4;
+            const int bsh = bs_sh < 6 ? bs_sh : 6, csh = bsh - kEsh;
 #pragma unroll
-              for (int q = 0; q < kEpc / 2; q++)
-                h[q] &= (read_tok(t0c + 2 * q) ? 0x0000ffffu : 0u) | (read_tok(t0c + 2 * q + 1) ? 0xffff0000u : 0u);
+            for (int i = 0; i < kPer; i++) {
+              const int c = ct + 128 * i, rem = c & ((D << csh) - 1), d = rem >> csh;
+              const int t0c = ((c >> (kDsh + csh)) << bsh) + ((rem & ((1 << csh) - 1)) << kEsh);   // first token
+              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+              uint32_t h[8];
+              if constexpr (!k16) {
+                if constexpr (kKv == kKvE4m3) {
+#pragma unroll
+                  for (int q = 0; q < 8; q++) h[q] = e4m3x2_to_f16x2((uint16_t)(ws[q >> 1] >> (16 * (q & 1))));
+                } else {
+#pragma unroll
+                  for (int q = 0; q < 8; q++) {
+                    const uint32_t x = __byte_perm(ws[q >> 1] ^ 0x80808080u, 0x64646464u, (q & 1) ? 0x5342u : 0x5140u);
+                    const __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+                    h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < 4; q++) h[q] = ws[q];
+              }
+              if constexpr (kKv != kKvI8) {
+#pragma unroll
+                for (int q = 0; q < kEpc / 2; q++)
+                  h[q] &= (read_tok(t0c + 2 * q) ? 0x0000ffffu : 0u) | (read_tok(t0c + 2 * q + 1) ? 0xffff0000u : 0u);
+              }
+              const uint32_t a0 = dst + (t0c >> 3) * (16 * D) + 16 * d;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                           "r"(h[3]));
+              if constexpr (!k16)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 16 * D), "r"(h[4]), "r"(h[5]),
+                             "r"(h[6]), "r"(h[7]));
             }
-            const uint32_t a0 = dst + (t0c >> 3) * (16 * D) + 16 * d;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                         "r"(h[3]));
-            if constexpr (!k16)
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 16 * D), "r"(h[4]), "r"(h[5]),
-                           "r"(h[6]), "r"(h[7]));
           }
         } else {
 #pragma unroll
@@ -924,7 +967,7 @@ bool encode_i8_map(CUtensorMap* map, const void* base, int64_t rows, int inner, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int kKv, bool kVdm>
+template <int D, int kKv, int kVL>
 cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   constexpr int kEsz = (kKv == kKvF16 || kKv == kKvBf16) ? 2 : 1;
   using S = Lay<D, kEsz, kKv == kKvBf16 ? 2 : 1>;
@@ -933,28 +976,31 @@ cudaError_t launch_d(const Params& p, cudaStream_t stream) {
   const int box_rows = p.bs < kT ? p.bs : kT;
   if (!encode_i8_map(&km, p.k_cache, rows, D, box_rows, kEsz)) return cudaErrorInvalidValue;
   // dimension-major V: [pages * Hkv * D rows][bs tokens], a box of box_rows tokens x D rows
-  if (kVdm ? !encode_i8_map(&vm, p.v_cache, (int64_t)p.num_pages * p.Hkv * D, p.bs, D, kEsz, box_rows)
+  // (no map for 8-byte dim rows, which the kernel copies page by page)
+  memset(&vm, 0, sizeof(vm));
+  if (kVL != kVTok ? kVL == kVDim && !encode_i8_map(&vm, p.v_cache, (int64_t)p.num_pages * p.Hkv * D, p.bs, D, kEsz,
+                                                box_rows)
            : !encode_i8_map(&vm, p.v_cache, rows, D, box_rows, kEsz))
     return cudaErrorInvalidValue;
   constexpr int smem = (int)S::kSmem;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kKv, kVdm>), smem);
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&partial_tc_i8_kernel<D, kKv, kVL>), smem);
   if (e != cudaSuccess) return e;
   const int n_items = p.B * p.Hkv * p.num_splits;
   const int n_sm = sm_count();
   if (n_sm <= 0) return cudaErrorInvalidValue;
   dim3 grid(n_items < n_sm ? n_items : n_sm);
-  partial_tc_i8_kernel<D, kKv, kVdm><<<grid, kThreads, smem, stream>>>(p, km, vm);
+  partial_tc_i8_kernel<D, kKv, kVL><<<grid, kThreads, smem, stream>>>(p, km, vm);
   return cudaGetLastError();
 }
 
-template <int kKv, bool kVdm>
+template <int kKv, int kVL>
 cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
   switch (p.D) {
-    case 64: return launch_d<64, kKv, kVdm>(p, stream);
-    case 128: return launch_d<128, kKv, kVdm>(p, stream);
+    case 64: return launch_d<64, kKv, kVL>(p, stream);
+    case 128: return launch_d<128, kKv, kVL>(p, stream);
     case 256:
       // a 16-bit tile of head_dim 256 would not leave room for the staging rings and f16 buffers
-      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv, kVdm>(p, stream);
+      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv, kVL>(p, stream);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
@@ -962,7 +1008,10 @@ cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
 
 template <int kKv>
 cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
-  return p.v_dim_major ? launch_kv<kKv, true>(p, stream) : launch_kv<kKv, false>(p, stream);
+  if (!p.v_dim_major) return launch_kv<kKv, kVTok>(p, stream);
+  if constexpr (kKv == kKvI8 || kKv == kKvE4m3)
+    if (p.bs < 16) return launch_kv<kKv, kVDim8>(p, stream);
+  return launch_kv<kKv, kVDim>(p, stream);
 }
 
 }  // namespace
@@ -971,8 +1020,7 @@ bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const int bs = d.block_size;
   const bool quant = d.kv_dtype == TLLM_INT8 || d.kv_dtype == TLLM_FP8_E4M3;
   const bool b16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
-  // a transposed V cache: a page's dimension row must be a whole number of 16-byte chunks
-  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || (d.v_layout == TLLM_V_DIM_MAJOR && (b16 || bs >= 16));
+  const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || d.v_layout == TLLM_V_DIM_MAJOR;
   return (quant || b16) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
          (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && quant)) && v_ok &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&

@@ -307,21 +307,21 @@ def test_contiguous_cache_needs_every_request_block(lib):
 def test_dim_major_v_routes_to_kernels_that_read_it(lib):
     """AUTO with a transposed V cache: the FP8 tensor-core kernel for FP8 KV (head_dim 128, pages
     of 16 or more tokens, at most 64 rows); the widening tensor-core kernel for more than 8 rows
-    of the other quantised shapes (pages of 16 or more tokens) and of 16-bit caches up to
-    head_dim 128; the pipelined CUDA-core kernel for the rest, except 8-bit caches with 8-token
-    pages, which the generic kernel reads."""
+    of the other quantised shapes (8-token pages included) and of 16-bit caches up to head_dim
+    128; the pipelined CUDA-core kernel for the rest."""
     def plan(wl):
         return B.tllm_decode_attn_plan(B.desc_for(wl, v_layout=B.TLLM_V_DIM_MAJOR), wl.B, wl.Lq, 0,
                                        host_ctx_lens=wl.ctx)
     assert plan(W.mtp4_fp8_long(batch=2, ctx=4000)).kernel == B.TLLM_KERNEL_TC_FP8
-    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000, bs=8)).kernel == B.TLLM_KERNEL_GENERIC
+    assert plan(W.mtp4_fp8_long(batch=2, ctx=4000, bs=8)).kernel == B.TLLM_KERNEL_TC_I8
     assert plan(W.window_sink_bf16(batch=2)).kernel == B.TLLM_KERNEL_SIMT
     assert plan(W.window_sink_bf16(batch=2).replace(bs=8, D=256, Hq=32, Hkv=2)).kernel == B.TLLM_KERNEL_SIMT
     assert plan(W.verify16_int8()).kernel == B.TLLM_KERNEL_TC_I8
     assert plan(W.mtp4_fp8_long(batch=2, ctx=4000).replace(D=64)).kernel == B.TLLM_KERNEL_TC_I8
     assert plan(W.window_sink_bf16(batch=2).replace(bs=8, D=128, Hq=32, Hkv=2)).kernel == B.TLLM_KERNEL_TC_I8
     assert plan(W.verify16_int8().replace(Lq=1)).kernel == B.TLLM_KERNEL_SIMT        # 6 rows
-    assert plan(W.verify16_int8().replace(bs=8)).kernel == B.TLLM_KERNEL_GENERIC
+    assert plan(W.verify16_int8().replace(bs=8)).kernel == B.TLLM_KERNEL_TC_I8
+    assert plan(W.verify16_int8().replace(bs=8, Lq=1)).kernel == B.TLLM_KERNEL_SIMT
 
 
 def test_sixteen_bit_records_halve_the_record_area(lib):
@@ -375,6 +375,22 @@ def test_auto_never_falls_back_for_quantised_caches(lib, kv, D):
         assert k != B.TLLM_KERNEL_GENERIC, (kv, D, G * Lq)
         if G * Lq > 8:
             assert k in (B.TLLM_KERNEL_TC_FP8, B.TLLM_KERNEL_TC_I8), (kv, D, G * Lq, k)
+
+
+@pytest.mark.parametrize("v_layout", [B.TLLM_V_TOKEN_MAJOR, B.TLLM_V_DIM_MAJOR])
+@pytest.mark.parametrize("kv", ["e4m3", "i8", "f16", "bf16"])
+def test_auto_never_falls_back_for_any_page_size_or_v_layout(lib, kv, v_layout):
+    """Every cache type, head_dim, page size (8 to 128 tokens) and V layout, with 1 to 128
+    packed rows and either 16-bit query: AUTO never picks the generic kernel."""
+    for D in (64, 128, 256):
+        for bs in (8, 16, 32, 64, 128):
+            for q in ("bf16", "f16"):
+                for G, Lq in ((1, 1), (7, 1), (8, 1), (4, 4), (16, 4), (6, 16), (8, 16)):
+                    wl = W.mtp4_fp8_long(batch=2, ctx=1000).replace(Hq=G, Hkv=1, Lq=Lq, D=D, bs=bs, kv_dtype=kv,
+                                                                    q_dtype=q)
+                    desc = B.desc_for(wl, v_layout=v_layout)
+                    k = B.tllm_decode_attn_plan(desc, wl.B, wl.Lq, 0, host_ctx_lens=wl.ctx).kernel
+                    assert k != B.TLLM_KERNEL_GENERIC, (kv, q, D, bs, G * Lq, v_layout)
 
 
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("f16", "f16"), ("f16", "bf16"), ("bf16", "f16")])

@@ -768,7 +768,7 @@ def test_dim_major_v_cache(bs, kernel):
 @pytest.mark.parametrize("kv_dtype,q_dtype,D,bs,Hq,Hkv,Lq", [
     ("f16", "f16", 64, 8, 14, 2, 1), ("bf16", "bf16", 128, 16, 32, 8, 1), ("bf16", "bf16", 256, 32, 32, 2, 1),
     ("i8", "bf16", 256, 16, 24, 4, 16), ("e4m3", "bf16", 64, 64, 16, 1, 4), ("i8", "f16", 128, 128, 8, 2, 2),
-    ("f16", "bf16", 128, 16, 12, 4, 3),
+    ("f16", "bf16", 128, 16, 12, 4, 3), ("i8", "bf16", 128, 8, 8, 2, 1), ("e4m3", "f16", 256, 8, 16, 2, 2),
 ])
 def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
     """The pipelined CUDA-core kernel on a transposed V cache (AUTO's choice for 8 rows or fewer
@@ -798,13 +798,15 @@ def test_dim_major_v_cuda_core_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
     ("i8", "bf16", 256, 16, 24, 4, 16), ("e4m3", "bf16", 64, 64, 16, 1, 4), ("i8", "f16", 128, 128, 8, 2, 4),
     ("f16", "f16", 64, 8, 14, 2, 2), ("bf16", "bf16", 128, 16, 32, 8, 4), ("bf16", "bf16", 64, 32, 32, 2, 2),
     ("f16", "f16", 128, 128, 12, 4, 3), ("e4m3", "f16", 128, 32, 16, 2, 8), ("i8", "bf16", 64, 16, 16, 1, 8),
-    ("e4m3", "bf16", 256, 16, 8, 1, 1),
+    ("e4m3", "bf16", 256, 16, 8, 1, 1), ("i8", "bf16", 256, 8, 24, 4, 16), ("e4m3", "bf16", 128, 8, 16, 2, 4),
+    ("i8", "f16", 64, 8, 8, 1, 2),
 ])
 def test_dim_major_v_widening_kernel(kv_dtype, q_dtype, D, bs, Hq, Hkv, Lq):
     """The widening tensor-core kernel on a transposed V cache (AUTO's choice past 8 rows where
     the FP8 kernel does not apply): each page's [D, bs] block is staged as it lies and widened
     into the K-major f16 operand of the PV product. Every cache type, head_dim 64 to 256, pages
-    of 8 to 128 tokens, 8 to 128 rows, with a window, sinks, ragged lengths and poisoned tails
+    of 8 to 128 tokens (8-bit 8-token pages copied whole, two dims per 16-byte chunk), 8 to 128
+    rows, with a window, sinks, ragged lengths and poisoned tails
     and pages (whose NaN codes must not reach the product)."""
     wl = W.verify16_int8().replace(ctx=[3000, 700, 65, 9], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, bs=bs, kv_dtype=kv_dtype,
                                    q_dtype=q_dtype, window=900, sinks=True, extra_pages=4,
