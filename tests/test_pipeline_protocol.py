@@ -32,7 +32,10 @@ class Bar:
         self.done += 1
 
 
-def roles(n, rnd, rescale_p, skip_v_wait=False):
+def roles(n, rnd, rescale_p, skip_v_wait=False, sk=SK, sv=SV, nk16=2, v_wait_at_v=False):
+    """The widening kernel: staging rings of depth sk (K) and sv (V), nk16 f16 K buffers; with
+    v_wait_at_v the converters wait for a staged V tile when they widen it instead of before
+    widening the K tile of the same index (the 16-bit caches, which read no V scales)."""
     def prod(name, depth):
         for j in range(n):
             st = j % depth
@@ -46,31 +49,33 @@ def roles(n, rnd, rescale_p, skip_v_wait=False):
         for step in range(n + 1):
             if step < n:
                 j = step
-                yield ("wait", f"fK8{j % SK}", j // SK)
-                yield ("wait", f"fV8{j % SV}", j // SV)
+                yield ("wait", f"fK8{j % sk}", j // sk)
+                if not v_wait_at_v:
+                    yield ("wait", f"fV8{j % sv}", j // sv)
                 yield ("arrive", f"meta{j % 4}")
-                if j >= 2:
-                    yield ("wait", f"eK16{j & 1}", (j >> 1) - 1)
-                yield ("arrive", f"fK16{j & 1}")
-                yield ("arrive", f"eK8{j % SK}")
+                if j >= nk16:
+                    yield ("wait", f"eK16{j % nk16}", j // nk16 - 1)
+                yield ("arrive", f"fK16{j % nk16}")
+                yield ("arrive", f"eK8{j % sk}")
             if step >= 1:
                 j = step - 1
+                if v_wait_at_v:
+                    yield ("wait", f"fV8{j % sv}", j // sv)
                 if j >= 1 and not skip_v_wait:
                     yield ("wait", "eV16", j - 1)
                 yield ("arrive", "fV16")
-                yield ("arrive", f"eV8{j % SV}")
-        yield ("wait", f"eK16{(n - 1) & 1}", (n - 1) >> 1)
-        if n >= 2:
-            yield ("wait", f"eK16{(n - 2) & 1}", (n - 2) >> 1)
+                yield ("arrive", f"eV8{j % sv}")
+        for j in range(max(0, n - nk16), n):
+            yield ("wait", f"eK16{j % nk16}", j // nk16)
         yield ("wait", "eV16", n - 1)
 
     def qk():
         yield ("wait", "q", 0)
         for j in range(n):
-            yield ("wait", f"fK16{j & 1}", j >> 1)
+            yield ("wait", f"fK16{j % nk16}", j // nk16)
             if j >= 2:
                 yield ("wait", f"sfree{j & 1}", (j >> 1) - 1)
-            yield ("async", [f"sfull{j & 1}", f"eK16{j & 1}"])
+            yield ("async", [f"sfull{j & 1}", f"eK16{j % nk16}"])
 
     def pv():
         for j in range(n):
@@ -96,7 +101,7 @@ def roles(n, rnd, rescale_p, skip_v_wait=False):
         if last >= 0:
             yield ("wait", f"pv{last & 1}", last >> 1)
 
-    return {"prodK": prod("K", SK), "prodV": prod("V", SV), "conv": conv(), "qk": qk(), "pv": pv(),
+    return {"prodK": prod("K", sk), "prodV": prod("V", sv), "conv": conv(), "qk": qk(), "pv": pv(),
             "soft": soft()}
 
 
@@ -221,7 +226,7 @@ def b16_roles(n, rnd, p_rare):
     return actors
 
 
-def run(n, seed, rescale_p=0.3, skip_v_wait=False, model="widening", skip_p_wait=False):
+def run(n, seed, rescale_p=0.3, skip_v_wait=False, model="widening", skip_p_wait=False, **shape):
     rnd = random.Random(seed)
     bars = {}
     counts = {"fp8": FP8_COUNTS, "b16": B16_COUNTS}.get(model, {})
@@ -232,7 +237,7 @@ def run(n, seed, rescale_p=0.3, skip_v_wait=False, model="widening", skip_p_wait
         return bars[name]
 
     if model == "widening":
-        actors = roles(n, rnd, rescale_p, skip_v_wait)
+        actors = roles(n, rnd, rescale_p, skip_v_wait, **shape)
     elif model == "fp8":
         actors = fp8_roles(n, rnd, rescale_p, skip_p_wait)
     else:
@@ -297,3 +302,20 @@ def test_the_fp8_protocol_check_catches_a_missing_wait():
 def test_sixteen_bit_kernel_barrier_protocol(n):
     for seed in range(100):
         run(n, 15485863 * n + seed, model="b16")
+
+
+@pytest.mark.parametrize("nk16", [1, 2])
+@pytest.mark.parametrize("n", list(range(1, 13)))
+def test_widening_kernel_one_deep_rings(n, nk16):
+    """The 16-bit head_dim-256 instance of the widening kernel: one-deep K and V staging rings,
+    one or two f16 K buffers, and the staged V tile waited for when it is widened."""
+    for seed in range(60):
+        run(n, 104729 * n + seed, sk=1, sv=1, nk16=nk16, v_wait_at_v=True)
+
+
+def test_one_deep_v_ring_needs_the_v_wait_at_v():
+    """Waiting for V(j) before widening K(j), as the deeper rings do, deadlocks a one-deep V
+    ring: V(j) cannot land before V(j - 1) is widened, which comes after K(j)."""
+    with pytest.raises(AssertionError, match="deadlock"):
+        for seed in range(50):
+            run(3, seed, sk=1, sv=1, nk16=1, v_wait_at_v=False)
