@@ -84,11 +84,16 @@ struct Lay {
   static constexpr uint32_t kMeta = kSc + 16;                 // scales | page mask | largest V scale x2
   static constexpr uint32_t kRaw = kT * D * kEsz;             // one staged operand tile (K or V) as stored
   static constexpr uint32_t kStage = align1k(kRaw + kScT + 16);        // rows | scales | page mask, as stored
-  static constexpr int kStK = 2, kStV = 3;                    // staging ring depths: K, V
+  // A 16-bit tile of head_dim 256 is 32 KB: that instance stages K and V one tile deep (the
+  // converters then wait for a staged V tile when they widen it, not before its K tile) and,
+  // for bf16 (two P parts), keeps one f16 K buffer, so that the stages fit the shared memory.
+  static constexpr bool kBig16 = D == 256 && kEsz == 2;
+  static constexpr int kStK = kBig16 ? 1 : 2, kStV = kBig16 ? 1 : 3;   // staging ring depths: K, V
+  static constexpr int kNK16 = kBig16 && kPParts == 2 ? 1 : 2;         // f16 K buffers
   static constexpr uint32_t kHalf16 = kT * D * 2;                      // one f16 tile (K or V)
   static constexpr uint32_t kOff8 = 0;                        // the staging rings: K, then V
   static constexpr uint32_t kOffK8 = 0, kOffV8 = kStK * kStage, kOff16 = kOffV8 + kStV * kStage;
-  static constexpr uint32_t kOffP = kOff16 + 3 * kHalf16;     // f16 stage: K buffer 0 | K buffer 1 | V
+  static constexpr uint32_t kOffP = kOff16 + (kNK16 + 1) * kHalf16;   // f16 stage: K buffer(s) | V
   static constexpr uint32_t kPPart = 128 * 128;               // P: 128 rows x 64 tokens, 16-bit
   static constexpr uint32_t kPBuf = kPPart * kPParts;         // (bf16 V: high part | low part)
   static constexpr uint32_t kOffMeta = kOffP + 2 * kPBuf;     // meta ring: 4 tiles
@@ -324,23 +329,24 @@ __global__ void __launch_bounds__(kThreads)
         ok = mbar_wait(bars.q_full(), 0, abort);
         // (a failure-detection test stalls here: no QK^T, so every wait on S runs out)
         for (int j = 0; ok && j < n_tiles && !p.test_stall; j++) {
-          const int sb = j & 1;                            // S buffer and f16 K buffer of tile j
-          if (!mbar_wait(bars.fullK16(sb), (j >> 1) & 1, abort)) { ok = false; break; }
+          const int sb = j & 1;                            // S buffer (and f16 K buffer) of tile j
+          const int kb = S::kNK16 == 2 ? sb : 0;
+          if (!mbar_wait(bars.fullK16(kb), (S::kNK16 == 2 ? j >> 1 : j) & 1, abort)) { ok = false; break; }
           if (j >= 2 && !mbar_wait(bars.s_free(sb), ((j >> 1) - 1) & 1, abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sbase + S::kOff16 + sb * S::kHalf16;
+          const uint32_t kt = sbase + S::kOff16 + kb * S::kHalf16;
 #pragma unroll
           for (int k = 0; k < D / 16; k++)
             mma_f16_ts(tmem + kColS + 64 * sb, tmem + kColQ + 8 * k,
                        sdesc_sw128(kt + (k >> 2) * S::kAtom + 32 * (k & 3), 16, 1024), idqk, k > 0 ? 1u : 0u);
           mma_commit(bars.s_full(sb));
-          mma_commit(bars.emptyK16(sb));
+          mma_commit(bars.emptyK16(kb));
         }
       } else {
         // P and V in f16 (bf16 V: both bf16); V MN-major as widened from token-major pages, K-major
         // (8-token blocks of D rows x 16 bytes) from dimension-major ones
         const uint32_t idpv = idesc_f16(128, D, kPParts - 1, 0, kVdm ? 0 : 1);
-        const uint32_t vt = sbase + S::kOff16 + 2 * S::kHalf16;
+        const uint32_t vt = sbase + S::kOff16 + S::kNK16 * S::kHalf16;
         for (int j = 0; ok && j < n_tiles; j++) {
           const int pb = j & 1;
           if (!mbar_wait(bars.p_full(pb), (j >> 1) & 1, abort)) { ok = false; break; }
@@ -386,8 +392,11 @@ __global__ void __launch_bounds__(kThreads)
         const uint8_t* srcv = sm + S::kOffV8 + stv * S::kStage;
         if (which == 0) {
           if (!mbar_wait(bars.fullK8(stk), (j / S::kStK) & 1, abort)) set_abort_i8(abort, p.status);
-          if (!mbar_wait(bars.fullV8(stv), (j / S::kStV) & 1, abort)) set_abort_i8(abort, p.status);
+          if constexpr (!S::kBig16)
+            if (!mbar_wait(bars.fullV8(stv), (j / S::kStV) & 1, abort)) set_abort_i8(abort, p.status);
         }
+        if constexpr (S::kBig16)                           // (one-deep V ring: V(j) lands after V(j - 1) is widened)
+          if (which == 1 && !mbar_wait(bars.fullV8(stv), (j / S::kStV) & 1, abort)) set_abort_i8(abort, p.status);
         const uint8_t* src = which == 0 ? srck : srcv;     // (the K stage is not read for V: it may hold tile j + 2)
         const uint32_t pmask8 = *reinterpret_cast<const volatile uint32_t*>(src + S::kRaw + S::kScT);
         const int tt = t0 + j * kT;
@@ -398,8 +407,11 @@ __global__ void __launch_bounds__(kThreads)
           return ((pmask8 >> slot) & 1) && tt + t >= vlo && tt + t < t1;
         };
         // this thread's chunks of the operand, loaded before anything is converted (their
-        // latencies overlap)
-        uint4 w[kPer];
+        // latencies overlap); a 16-bit tile of head_dim 256 (16 chunks a thread) is loaded and
+        // stored below in two batches of 8, within the register budget
+        constexpr int kBatch = S::kBig16 ? 8 : kPer;
+        uint4 w[kBatch];
+        if constexpr (!S::kBig16)
 #pragma unroll
         for (int i = 0; i < kPer; i++) {
           const int c = ct + 128 * i, t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
@@ -420,7 +432,12 @@ __global__ void __launch_bounds__(kThreads)
           for (int i = 0; i < kPer; i++) {
             const int t = (ct + 128 * i) / kChunksPerRow;
             if (read_tok(t)) {
-              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+              uint4 x;
+              if constexpr (S::kBig16)
+                x = *reinterpret_cast<const uint4*>(src + (t * D + ((ct + 128 * i) % kChunksPerRow) * kEpc) * kEsz);
+              else
+                x = w[i];
+              const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int k = 0; k < 4; k++)
                 mx = fmax3(mx, fabsf(__uint_as_float(ws[k] << 16)), fabsf(__uint_as_float(ws[k] & 0xffff0000u)));
@@ -455,15 +472,49 @@ __global__ void __launch_bounds__(kThreads)
           __syncwarp();
           if (lane == 0) mbar_arrive(bars.meta_full(j & 3));
         }
-        // f16 K buffer j % 2 is free once the QK^T of tile j - 2 is done; the V buffer once the
-        // PV of tile j - 1 is done
-        if (which == 0 ? (j >= 2 && !mbar_wait(bars.emptyK16(j & 1), ((j >> 1) - 1) & 1, abort))
+        // f16 K buffer j % 2 is free once the QK^T of tile j - 2 is done (with one K buffer: of
+        // tile j - 1); the V buffer once the PV of tile j - 1 is done
+        const int kb = S::kNK16 == 2 ? (j & 1) : 0;        // (K) its f16 buffer
+        if (which == 0 ? (j >= S::kNK16 && !mbar_wait(bars.emptyK16(kb), (S::kNK16 == 2 ? (j >> 1) - 1 : j - 1) & 1,
+                                                      abort))
                        : (j >= 1 && !mbar_wait(bars.emptyV16(), (j - 1) & 1, abort)))
           set_abort_i8(abort, p.status);
-        const uint32_t dst = sbase + S::kOff16 + (which == 0 ? (j & 1) : 2) * S::kHalf16;
+        const uint32_t dst = sbase + S::kOff16 + (which == 0 ? kb : S::kNK16) * S::kHalf16;
         const __half2 bias = __half2(__half_raw{0x6480}, __half_raw{0x6480});
         const float emul = __int_as_float((e + 127) << 23);
-        if (kVdm && which == 1) {
+        if constexpr (S::kBig16) {
+          // a 16-bit tile of head_dim 256 (token-major V only): the same copy as below, in two
+          // batches of 8 chunks a thread
+#pragma unroll
+          for (int b0 = 0; b0 < kPer; b0 += kBatch) {
+#pragma unroll
+            for (int i = 0; i < kBatch; i++) {
+              const int c = ct + 128 * (b0 + i), t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+              w[i] = *reinterpret_cast<const uint4*>(src + (t * D + d0) * kEsz);
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; i++) {
+              const int c = ct + 128 * (b0 + i), t = c / kChunksPerRow, d0 = (c % kChunksPerRow) * kEpc;
+              const bool ok = which == 0 || read_tok(t);   // (V rows of unread tokens become zero)
+              const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+              const uint32_t base = dst + (d0 >> 6) * S::kAtom;
+              const uint32_t byte = (d0 & 63) * 2;
+              uint32_t h[4];
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                if (kKv == kKvBf16 && which == 0) {
+                  const __half2 v2 = __floats2half2_rn(__uint_as_float(ws[q] << 16) * emul,
+                                                       __uint_as_float(ws[q] & 0xffff0000u) * emul);
+                  h[q] = *reinterpret_cast<const uint32_t*>(&v2);
+                } else {
+                  h[q] = ok ? ws[q] : 0u;
+                }
+              }
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(t, byte)), "r"(h[0]),
+                           "r"(h[1]), "r"(h[2]), "r"(h[3]));
+            }
+          }
+        } else if (kVdm && which == 1) {
           // dimension-major V: chunk c holds kEpc tokens of one dim of one page slot; widened,
           // they go to the K-major f16 V buffer, whose 8-token blocks are D rows x 16 bytes.
           // Tokens the split does not read are zeroed element by element (e4m3 and 16-bit codes
@@ -588,7 +639,7 @@ __global__ void __launch_bounds__(kThreads)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(which == 0 ? bars.fullK16(j & 1) : bars.fullV16());
+          mbar_arrive(which == 0 ? bars.fullK16(kb) : bars.fullV16());
           mbar_arrive(which == 0 ? bars.emptyK8(stk) : bars.emptyV8(stv));
         }
       }
@@ -596,8 +647,13 @@ __global__ void __launch_bounds__(kThreads)
     // the releases of the f16 buffers by the last tiles' MMAs (asynchronous tcgen05.commit
     // arrivals) must have landed before the next item re-initialises the barriers
     const int nl = n_tiles - 1;
-    if (!mbar_wait(bars.emptyK16(nl & 1), (nl >> 1) & 1, abort)) set_abort_i8(abort, p.status);
-    if (nl >= 1 && !mbar_wait(bars.emptyK16((nl - 1) & 1), ((nl - 1) >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+    if constexpr (S::kNK16 == 2) {
+      if (!mbar_wait(bars.emptyK16(nl & 1), (nl >> 1) & 1, abort)) set_abort_i8(abort, p.status);
+      if (nl >= 1 && !mbar_wait(bars.emptyK16((nl - 1) & 1), ((nl - 1) >> 1) & 1, abort))
+        set_abort_i8(abort, p.status);
+    } else {
+      if (!mbar_wait(bars.emptyK16(0), nl & 1, abort)) set_abort_i8(abort, p.status);
+    }
     if (!mbar_wait(bars.emptyV16(), nl & 1, abort)) set_abort_i8(abort, p.status);
   } else if (warp >= 4) {
     // ---------------- softmax: two threads per packed row r (TMEM lane), one per token half ----------------
@@ -999,8 +1055,8 @@ cudaError_t launch_kv(const Params& p, cudaStream_t stream) {
     case 64: return launch_d<64, kKv, kVL>(p, stream);
     case 128: return launch_d<128, kKv, kVL>(p, stream);
     case 256:
-      // a 16-bit tile of head_dim 256 would not leave room for the staging rings and f16 buffers
-      if constexpr (kKv == kKvI8 || kKv == kKvE4m3) return launch_d<256, kKv, kVL>(p, stream);
+      // a 16-bit cache at head_dim 256: token-major V only (one-deep rings, batched widening)
+      if constexpr (kKv == kKvI8 || kKv == kKvE4m3 || kVL == kVTok) return launch_d<256, kKv, kVL>(p, stream);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
@@ -1022,7 +1078,8 @@ bool tc_i8_supports(const tllm_decode_attn_desc& d, int rows) {
   const bool b16 = d.kv_dtype == TLLM_F16 || d.kv_dtype == TLLM_BF16;
   const bool v_ok = d.v_layout == TLLM_V_TOKEN_MAJOR || d.v_layout == TLLM_V_DIM_MAJOR;
   return (quant || b16) && (d.q_dtype == TLLM_BF16 || d.q_dtype == TLLM_F16) &&
-         (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && quant)) && v_ok &&
+         (d.head_dim == 64 || d.head_dim == 128 || (d.head_dim == 256 && (quant || d.v_layout == TLLM_V_TOKEN_MAJOR))) &&
+         v_ok &&
          rows >= 1 && rows <= 128 && (bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128) &&
          (int64_t)d.num_pages * d.num_kv_heads * bs < ((int64_t)1 << 31) &&
          (int64_t)d.num_pages * d.num_kv_heads * d.head_dim < ((int64_t)1 << 31);   // (a transposed V's rows)

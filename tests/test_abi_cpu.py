@@ -184,7 +184,7 @@ def test_plan_rejects_bad_call_shape(lib):
     (W.window_sink_bf16().replace(Hq=16, Hkv=1), B.TLLM_KERNEL_TC_B16),                   # 16 rows
     (W.window_sink_bf16().replace(Hq=4, Hkv=1, Lq=4), B.TLLM_KERNEL_TC_B16),              # 16 rows
     (W.window_sink_bf16().replace(Hq=32, Hkv=1), B.TLLM_KERNEL_TC_I8),                    # 32 rows
-    (W.window_sink_bf16().replace(Hq=32, Hkv=1, D=256), B.TLLM_KERNEL_SIMT),              # 32 rows, D 256
+    (W.window_sink_bf16().replace(Hq=32, Hkv=1, D=256), B.TLLM_KERNEL_TC_I8),             # 32 rows, D 256
     (W.window_sink_bf16().replace(kv_dtype="f16"), B.TLLM_KERNEL_SIMT),                   # bf16 Q, f16 KV
     (W.window_sink_bf16().replace(q_dtype="f16", kv_dtype="f16", out_dtype="f16"), B.TLLM_KERNEL_TC_B16),
     (W.window_sink_bf16().replace(D=256), B.TLLM_KERNEL_SIMT),
@@ -192,8 +192,8 @@ def test_plan_rejects_bad_call_shape(lib):
 def test_auto_kernel_choice(lib, wl, kernel):
     """AUTO takes the FP8 tensor-core kernel for e4m3 KV at head_dim 128, the 16-bit one for
     f16/bf16 KV with a query of the same type, head_dim 128 and at most 16 packed rows, the
-    widening one for int8 KV, and for other 16-bit shapes up to head_dim 128, with more than 8
-    rows, then the CUDA-core kernels."""
+    widening one for int8 KV, and for other 16-bit shapes with more than 8 rows, then the
+    CUDA-core kernels."""
     p = _plan(wl, host_ctx_lens=wl.ctx)
     assert p.kernel == kernel
 
@@ -397,10 +397,10 @@ def test_auto_never_falls_back_for_any_page_size_or_v_layout(lib, kv, v_layout):
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_auto_never_falls_back_for_16bit_caches(lib, kv, q, D):
     """f16 and bf16 caches at every head_dim, up to 128 packed rows, with the query of either
-    16-bit type: AUTO picks a tensor-core kernel (or the pipelined CUDA-core kernel: for at most
-    8 rows, and in row blocks at head_dim 256, which no tensor-core kernel takes for 16-bit
-    caches), never the generic kernel; the 16-bit tensor-core kernel keeps the shapes it takes
-    (same query and cache type, head_dim 128, at most 16 rows)."""
+    16-bit type: AUTO picks a tensor-core kernel for more than 8 rows (the widening kernel,
+    head_dim 256 included) and the pipelined CUDA-core kernel for at most 8, never the generic
+    kernel; the 16-bit tensor-core kernel keeps the shapes it takes (same query and cache type,
+    head_dim 128, at most 16 rows)."""
     for G, Lq in ((1, 1), (7, 1), (4, 4), (8, 2), (8, 4), (24, 4), (6, 16), (8, 16)):
         wl = W.window_sink_bf16(batch=2).replace(Hq=G, Hkv=1, Lq=Lq, D=D, kv_dtype=kv, q_dtype=q)
         k = _plan(wl, host_ctx_lens=wl.ctx).kernel
@@ -408,9 +408,9 @@ def test_auto_never_falls_back_for_16bit_caches(lib, kv, q, D):
         assert k != B.TLLM_KERNEL_GENERIC, (kv, q, D, rows)
         if q == kv and D == 128 and rows <= 16:
             assert k == B.TLLM_KERNEL_TC_B16, (kv, q, D, rows, k)
-        elif rows > 8 and D < 256:
+        elif rows > 8:
             assert k == B.TLLM_KERNEL_TC_I8, (kv, q, D, rows, k)
-        elif D == 256:
+        else:
             assert k == B.TLLM_KERNEL_SIMT, (kv, q, D, rows, k)
 
 
@@ -418,10 +418,11 @@ def test_fused_combine_needs_one_row_block(lib):
     """The fused merge counts one arrival per split; with more than 8 rows the CUDA-core kernel
     runs several row blocks per split, so the plan keeps the combine kernel."""
     wl = W.window_sink_bf16(batch=2).replace(ctx=[2000, 900], Hq=32, Hkv=2, Lq=1, D=256)
-    d = B.desc_for(wl, combine_mode=B.TLLM_COMBINE_FUSED)
+    d = B.desc_for(wl, B.TLLM_KERNEL_SIMT, combine_mode=B.TLLM_COMBINE_FUSED)
     p = B.tllm_decode_attn_plan(d, wl.B, wl.Lq, wl.window, host_ctx_lens=wl.ctx, splits_override=4)
     assert p.kernel == B.TLLM_KERNEL_SIMT and p.fused_combine == 0
     wl8 = wl.replace(Hq=16)
-    p8 = B.tllm_decode_attn_plan(B.desc_for(wl8, combine_mode=B.TLLM_COMBINE_FUSED), wl8.B, wl8.Lq, wl8.window,
+    p8 = B.tllm_decode_attn_plan(B.desc_for(wl8, B.TLLM_KERNEL_SIMT, combine_mode=B.TLLM_COMBINE_FUSED), wl8.B,
+                                 wl8.Lq, wl8.window,
                                  host_ctx_lens=wl8.ctx, splits_override=4)
     assert p8.kernel == B.TLLM_KERNEL_SIMT and p8.fused_combine == 1

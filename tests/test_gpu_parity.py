@@ -267,6 +267,8 @@ def test_device_data_faults_set_status_and_stay_finite(kernel):
      B.TLLM_KERNEL_TC_I8),
     (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, Hq=32, Hkv=2, Lq=1, D=256, window=0, sinks=False),
      B.TLLM_KERNEL_SIMT),
+    (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, Hq=32, Hkv=2, Lq=1, D=256, window=0, sinks=False),
+     B.TLLM_KERNEL_TC_I8),
     (W.single_decode().replace(ctx=[1000] * 3), B.TLLM_KERNEL_SIMT),
     (W.window_sink_bf16(batch=3).replace(ctx=[1000] * 3, window=0, sinks=False), B.TLLM_KERNEL_TC_B16),
 ])
@@ -923,13 +925,15 @@ def test_widening_kernel_int8_head_dim_64(Hq, Hkv, Lq):
 
 # --- the widening kernel on 16-bit caches ----------------------------------------------
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("q_dtype,kv_dtype", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f16"), ("f16", "bf16")])
 @pytest.mark.parametrize("Hq,Hkv,Lq", [(24, 4, 16), (8, 1, 16), (32, 4, 2)])
 def test_widening_kernel_16bit_cache(Hq, Hkv, Lq, q_dtype, kv_dtype, D):
     """f16 caches copied and bf16 caches scaled into f16 by a power of two per tile: the shapes
-    the 16-bit tensor-core kernel does not take (more than 16 packed rows, head_dim 64, query and
-    cache of different types), with a window, sinks, ragged lengths and poisoned tails."""
+    the 16-bit tensor-core kernel does not take (more than 16 packed rows, head_dim 64 or 256,
+    query and cache of different types), with a window, sinks, ragged lengths and poisoned
+    tails. Head_dim 256 runs the instance with one-deep staging rings (and one f16 K buffer
+    for bf16)."""
     wl = W.window_sink_bf16(batch=4).replace(ctx=[3000, 700, 65, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=D, q_dtype=q_dtype,
                                              kv_dtype=kv_dtype, window=900, bs=16, extra_pages=4)
     inp = _inputs(wl, 240 + D + Hq + len(q_dtype + kv_dtype))
@@ -950,6 +954,21 @@ def test_widening_kernel_16bit_block_sizes(bs):
         out, plan, _ = run_gpu(inp, TCI8, splits=S)
         assert plan.kernel == TCI8
         assert_close(out, ref, wl.kv_dtype, f"widening bf16 bs{bs} S{S}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bs", [8, 64, 128])
+def test_widening_kernel_16bit_head_dim_256_block_sizes(bs, kv_dtype):
+    """Head_dim 256 with a 16-bit cache over many tiles per split (the one-deep rings' phases
+    cycle many times), pages of 8 to 128 tokens, a window and sinks."""
+    wl = W.window_sink_bf16(batch=3).replace(ctx=[6000, 333, 129], Hq=16, Hkv=1, Lq=2, D=256, bs=bs,
+                                             kv_dtype=kv_dtype, window=2500, extra_pages=3)
+    inp = _inputs(wl, 260 + bs + len(kv_dtype))
+    ref, _ = oracle_out(inp)
+    for S in (1, 5):
+        out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_AUTO, splits=S)
+        assert plan.kernel == TCI8
+        assert_close(out, ref, wl.kv_dtype, f"widening {kv_dtype} D256 bs{bs} S{S}")
 
 
 def test_widening_kernel_bf16_tile_magnitudes():
@@ -995,15 +1014,15 @@ def test_auto_takes_the_widening_kernel_for_16bit_caches(kv_dtype, D, Lq):
 @pytest.mark.parametrize("q_dtype,kv_dtype", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f16")])
 @pytest.mark.parametrize("Hq,Hkv,Lq", [(32, 4, 2), (16, 1, 4), (12, 4, 3)])
 def test_simt_row_blocks_head_dim_256_16bit(Hq, Hkv, Lq, q_dtype, kv_dtype):
-    """16-bit caches at head_dim 256 with 9..64 packed rows (no tensor-core kernel takes them):
-    AUTO runs the CUDA-core kernel in blocks of 8 rows, the last one ragged, with a window,
+    """16-bit caches at head_dim 256 with 9..64 packed rows on the CUDA-core kernel (pinned; AUTO
+    takes the widening kernel there), in blocks of 8 rows, the last one ragged, with a window,
     sinks, ragged lengths and poisoned tails."""
     wl = W.window_sink_bf16(batch=4).replace(ctx=[2600, 700, 65, 17], Hq=Hq, Hkv=Hkv, Lq=Lq, D=256, q_dtype=q_dtype,
                                              kv_dtype=kv_dtype, window=900, bs=16, extra_pages=4)
     inp = _inputs(wl, 280 + Hq + Lq + len(q_dtype + kv_dtype))
     ref, _ = oracle_out(inp)
     for S in (1, 3):
-        out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_AUTO, splits=S)
+        out, plan, _ = run_gpu(inp, B.TLLM_KERNEL_SIMT, splits=S)
         assert plan.kernel == B.TLLM_KERNEL_SIMT
         assert_close(out, ref, wl.kv_dtype, f"simt rows {Hq // Hkv * Lq} {kv_dtype} q {q_dtype} S{S}")
 
