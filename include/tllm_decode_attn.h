@@ -82,8 +82,8 @@ typedef enum {
   TLLM_KERNEL_SIMT = 2,              /* pipelined CUDA-core kernel, 8 packed rows per CTA */
   TLLM_KERNEL_TC_FP8 = 3,            /* tcgen05 FP8 kernel, e4m3 KV, head_dim 128 */
   TLLM_KERNEL_TC_I8 = 4,             /* tcgen05 16-bit kernel, bf16 / f16 Q, <= 128 rows: int8 or e4m3 KV
-                                        widened to f16 (head_dim 64 / 128 / 256), f16 / bf16 KV
-                                        (head_dim 64 / 128) */
+                                        widened to f16, f16 / bf16 KV (head_dim 64 / 128 / 256; a
+                                        16-bit cache at 256 with token-major V only) */
   TLLM_KERNEL_TC_B16 = 5             /* tcgen05 16-bit kernel, f16 / bf16 KV and Q, head_dim 128, <= 16 rows */
 } tllm_kernel;
 
